@@ -1,0 +1,338 @@
+"""Seeded synthetic workloads for paged-KV attention over working sets.
+
+This module makes INPUTS only: working-set shapes, operation scripts, token
+ids, free-page orders, FP8 scales and bf16 query/key/value draws.  It holds
+none of the attention or allocator arithmetic, and it is the only code that
+both the CPU oracle's tests and the CUDA path's tests and benchmark share.
+
+Value recipe: numpy ``PCG64`` seeded by a ``SeedSequence`` of
+(workload seed, stream id, layer, K/V/Q), fp32 draws of N(0, 1) rounded to
+bf16 (round to nearest even).  Token ids are uniform in [0, 128256) (the
+Llama 3 vocabulary size in "Write a model in Poem", section 1).  The free-page
+order is a seeded permutation.  FP8 scales are per (layer, KV head):
+``(4 + u) / 448`` with u uniform in [0, 1), so that about 4 to 5 standard
+deviations map to the largest E4M3 value.
+
+A workload is a list of operations on named working sets:
+
+    ("create", name)                 ("fork", parent, name)
+    ("freeze", name, n)              ("rollback", name, n)
+    ("match", name, token_stream)    ("destroy", name)
+    ("pass", segs, attend)
+
+where each seg of a pass is ``(name, n_new, kv_pieces, q_pieces, tok_pieces)``
+and a piece is ``(stream, start, count)``: the K/V (or Q, or token ids) of a
+segment are the concatenation of slices of named streams, so that forks and
+their unshared copies, or a rollback and its re-append, feed the same values.
+"""
+from __future__ import annotations
+
+import hashlib
+from dataclasses import dataclass, field
+
+import numpy as np
+
+KV_BF16 = 0
+KV_E4M3 = 1
+VOCAB = 128256
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def _stream_id(name: str) -> int:
+    return int.from_bytes(hashlib.sha256(name.encode()).digest()[:4], "little")
+
+
+def rng_for(seed: int, *key) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, *key])))
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    num_layers: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    kv_dtype: int
+    num_pages: int
+    ops: list
+    kv_streams: dict = field(default_factory=dict)     # name -> length
+    q_streams: dict = field(default_factory=dict)      # name -> length
+    tok_streams: dict = field(default_factory=dict)    # name -> length
+    page_size: int = 16
+    _cache: dict = field(default_factory=dict, repr=False)
+
+    # --------------------------------------------------------------- inputs
+    def free_list(self) -> np.ndarray:
+        return rng_for(self.seed, 100).permutation(self.num_pages).astype(np.int32)
+
+    def scales(self):
+        if self.kv_dtype != KV_E4M3:
+            return None, None
+        r = rng_for(self.seed, 200)
+        shape = (self.num_layers, self.num_kv_heads)
+        k = ((4.0 + r.random(shape)) / 448.0).astype(np.float32)
+        v = ((4.0 + r.random(shape)) / 448.0).astype(np.float32)
+        return k, v
+
+    def kv_stream(self, name: str, layer: int):
+        """(K, V) bf16 bits, each [length, Hkv, d]."""
+        key = ("kv", name, layer)
+        if key not in self._cache:
+            n = self.kv_streams[name]
+            shape = (n, self.num_kv_heads, self.head_dim)
+            sid = _stream_id(name)
+            k = bf16_round(rng_for(self.seed, sid, layer, 0).standard_normal(shape, dtype=np.float32))
+            v = bf16_round(rng_for(self.seed, sid, layer, 1).standard_normal(shape, dtype=np.float32))
+            self._cache[key] = (k, v)
+        return self._cache[key]
+
+    def q_stream(self, name: str, layer: int) -> np.ndarray:
+        key = ("q", name, layer)
+        if key not in self._cache:
+            n = self.q_streams[name]
+            shape = (n, self.num_q_heads, self.head_dim)
+            r = rng_for(self.seed, _stream_id(name), layer, 2)
+            self._cache[key] = bf16_round(r.standard_normal(shape, dtype=np.float32))
+        return self._cache[key]
+
+    def tok_stream(self, name: str) -> np.ndarray:
+        key = ("tok", name)
+        if key not in self._cache:
+            r = rng_for(self.seed, _stream_id(name), 3)
+            self._cache[key] = r.integers(0, VOCAB, self.tok_streams[name]).astype(np.int32)
+        return self._cache[key]
+
+    def gather_kv(self, pieces, layer: int):
+        ks, vs = [], []
+        for stream, start, count in pieces:
+            k, v = self.kv_stream(stream, layer)
+            ks.append(k[start:start + count])
+            vs.append(v[start:start + count])
+        return np.concatenate(ks), np.concatenate(vs)
+
+    def gather_q(self, pieces, layer: int) -> np.ndarray:
+        return np.concatenate([self.q_stream(s, layer)[a:a + c] for s, a, c in pieces])
+
+    def gather_tok(self, pieces):
+        if pieces is None:
+            return None
+        return np.concatenate([self.tok_stream(s)[a:a + c] for s, a, c in pieces])
+
+    def pass_inputs(self, segs, layer: int, attend: bool):
+        """Concatenated K, V (and Q) bf16 bits of a pass, in segment order."""
+        live = [s for s in segs if s[1] > 0]
+        k, v = zip(*(self.gather_kv(s[2], layer) for s in live)) if live else ((), ())
+        kk = np.concatenate(k) if k else np.zeros((0, self.num_kv_heads, self.head_dim), np.uint16)
+        vv = np.concatenate(v) if v else np.zeros((0, self.num_kv_heads, self.head_dim), np.uint16)
+        q = None
+        if attend:
+            qs = [self.gather_q(s[3], layer) for s in live]
+            q = np.concatenate(qs) if qs else np.zeros((0, self.num_q_heads, self.head_dim), np.uint16)
+        return kk, vv, q
+
+
+def _pages_for(lengths, page_size=16):
+    return int(sum(-(-n // page_size) for n in lengths))
+
+
+# ---------------------------------------------------------------- builders
+def tiny_decode() -> Workload:
+    """4 working sets, contexts {17, 33, 64, 100}; 8 query / 2 KV heads, d 64;
+    one layer; one decode token each, appended then attended."""
+    ctx = [17, 33, 64, 100]
+    ops = []
+    w = Workload("tiny_decode", 1, 1, 8, 2, 64, KV_BF16, 40, ops)
+    for i, n in enumerate(ctx):
+        ops.append(("create", f"w{i}"))
+        w.kv_streams[f"ctx{i}"] = n + 1
+        w.q_streams[f"q{i}"] = 1
+    ops.append(("pass", [(f"w{i}", n, [(f"ctx{i}", 0, n)], None, None) for i, n in enumerate(ctx)], False))
+    ops += [("freeze", f"w{i}", -1) for i in range(len(ctx))]
+    ops.append(("pass", [(f"w{i}", 1, [(f"ctx{i}", n, 1)], [(f"q{i}", 0, 1)], None)
+                         for i, n in enumerate(ctx)], True))
+    return w
+
+
+def decode_batch(name="llama8b_decode", seed=2, n_ws=64, ctx_lo=512, ctx_hi=8192,
+                 num_layers=32, hq=32, hkv=8, d=128, kv_dtype=KV_BF16,
+                 prefix_groups=0, prefix_len=0, slack_pages=64) -> Workload:
+    """Decode batch: n_ws working sets with contexts uniform in [ctx_lo, ctx_hi];
+    one new token each.  With prefix_groups > 0 the sets form that many equal
+    groups; in each, the first member writes and freezes a shared prefix of
+    prefix_len tokens (with token ids) and the others take it by match_prefix."""
+    r = rng_for(seed, 0)
+    ctx = r.integers(ctx_lo, ctx_hi + 1, n_ws).tolist()
+    ops = []
+    w = Workload(name, seed, num_layers, hq, hkv, d, kv_dtype, 0, ops)
+    gsize = n_ws // prefix_groups if prefix_groups else 0
+    for i in range(n_ws):
+        ops.append(("create", f"w{i}"))
+        w.q_streams[f"q{i}"] = 1
+    fill = []
+    if prefix_groups:
+        first = []
+        for g in range(prefix_groups):
+            w.kv_streams[f"pre{g}"] = prefix_len
+            w.tok_streams[f"pretok{g}"] = prefix_len
+            first.append((f"w{g * gsize}", prefix_len, [(f"pre{g}", 0, prefix_len)], None,
+                          [(f"pretok{g}", 0, prefix_len)]))
+        ops.append(("pass", first, False))
+        ops += [("freeze", f"w{g * gsize}", -1) for g in range(prefix_groups)]
+        for i in range(n_ws):
+            if i % gsize:
+                ops.append(("match", f"w{i}", f"pretok{i // gsize}"))
+    for i in range(n_ws):
+        own = ctx[i] - (prefix_len if prefix_groups else 0)
+        w.kv_streams[f"ctx{i}"] = own + 1
+        if own > 0:
+            fill.append((f"w{i}", own, [(f"ctx{i}", 0, own)], None, None))
+    ops.append(("pass", fill, False))
+    ops += [("freeze", f"w{i}", -1) for i in range(n_ws)]
+    own = [c - (prefix_len if prefix_groups else 0) for c in ctx]
+    ops.append(("pass", [(f"w{i}", 1, [(f"ctx{i}", own[i], 1)], [(f"q{i}", 0, 1)], None)
+                         for i in range(n_ws)], True))
+    unique = _pages_for([c + 1 for c in ctx])
+    if prefix_groups:
+        unique -= (n_ws - prefix_groups) * (prefix_len // 16)
+    w.num_pages = unique + slack_pages
+    w.ctx = ctx
+    return w
+
+
+def llama8b_decode(**kw) -> Workload:
+    """Llama-3.1-8B-shaped decode batch: 32 q / 8 KV heads, d 128, bf16,
+    64 working sets with contexts uniform in [512, 8192], 32 layers."""
+    return decode_batch(**kw)
+
+
+def llama70b_fp8(**kw) -> Workload:
+    """Llama-3.3-70B-shaped long-context decode with e4m3 KV: 64 q / 8 KV
+    heads, d 128, 256 working sets with contexts uniform in [2048, 32768],
+    groups of 8 sharing a deduplicated 2048-token prefix; one layer."""
+    args = dict(name="llama70b_fp8", seed=5, n_ws=256, ctx_lo=2048, ctx_hi=32768,
+                num_layers=1, hq=64, hkv=8, d=128, kv_dtype=KV_E4M3,
+                prefix_groups=32, prefix_len=2048)
+    args.update(kw)
+    return decode_batch(**args)
+
+
+def fork_spec(name="fork_spec", seed=3, prompt=4096, n_forks=10, suffix_hi=256, drafts=4,
+              rollback=2, num_layers=1, hq=32, hkv=8, d=128, unshared=True) -> Workload:
+    """One frozen prompt forked into n_forks working sets; each adds a frozen
+    suffix of 1..suffix_hi tokens and `drafts` speculative tokens that are
+    attended causally; then `rollback` drafts are dropped and re-appended
+    with the same values and attended again.  With `unshared`, the same
+    tokens are also built as independent copies that share nothing."""
+    r = rng_for(seed, 0)
+    suffix = r.integers(1, suffix_hi + 1, n_forks).tolist()
+    ops = []
+    w = Workload(name, seed, num_layers, hq, hkv, d, KV_BF16, 0, ops)
+    w.kv_streams["prompt"] = prompt
+    for i in range(n_forks):
+        w.kv_streams[f"suf{i}"] = suffix[i]
+        w.kv_streams[f"draft{i}"] = drafts
+        w.q_streams[f"dq{i}"] = drafts
+    ops.append(("create", "root"))
+    ops.append(("pass", [("root", prompt, [("prompt", 0, prompt)], None, None)], False))
+    ops.append(("freeze", "root", -1))
+    names = [f"f{i}" for i in range(n_forks)]
+    for n in names:
+        ops.append(("fork", "root", n))
+    ops.append(("pass", [(names[i], suffix[i], [(f"suf{i}", 0, suffix[i])], None, None)
+                         for i in range(n_forks)], False))
+    ops += [("freeze", n, -1) for n in names]
+    ops.append(("pass", [(names[i], drafts, [(f"draft{i}", 0, drafts)], [(f"dq{i}", 0, drafts)], None)
+                         for i in range(n_forks)], True))
+    ops += [("rollback", n, rollback) for n in names]
+    keep = drafts - rollback
+    ops.append(("pass", [(names[i], rollback, [(f"draft{i}", keep, rollback)],
+                          [(f"dq{i}", keep, rollback)], None) for i in range(n_forks)], True))
+    pages = _pages_for([prompt]) + _pages_for([prompt + s + drafts for s in suffix]) - n_forks * (prompt // 16)
+    if unshared:
+        copies = [f"u{i}" for i in range(n_forks)]
+        ops += [("create", c) for c in copies]
+        ops.append(("pass", [(copies[i], prompt + suffix[i],
+                              [("prompt", 0, prompt), (f"suf{i}", 0, suffix[i])], None, None)
+                             for i in range(n_forks)], False))
+        ops += [("freeze", c, -1) for c in copies]
+        ops.append(("pass", [(copies[i], drafts, [(f"draft{i}", 0, drafts)], [(f"dq{i}", 0, drafts)], None)
+                             for i in range(n_forks)], True))
+        pages += _pages_for([prompt + s + drafts for s in suffix])
+    w.num_pages = pages + n_forks * 2 + 16
+    w.suffix = suffix
+    return w
+
+
+def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=2048,
+                ctx_lo=0, ctx_hi=4096, n_decode=128, dec_lo=1, dec_hi=4096,
+                num_layers=1, hq=32, hkv=8, d=128) -> Workload:
+    """Mixed continuous batch: n_chunks prefill chunks of chunk_lo..chunk_hi new
+    tokens on existing contexts of ctx_lo..ctx_hi tokens, plus n_decode
+    single-token rows on contexts of dec_lo..dec_hi tokens, one attend call."""
+    r = rng_for(seed, 0)
+    chunk = r.integers(chunk_lo, chunk_hi + 1, n_chunks).tolist()
+    cctx = r.integers(ctx_lo, ctx_hi + 1, n_chunks).tolist()
+    dctx = r.integers(dec_lo, dec_hi + 1, n_decode).tolist()
+    ops = []
+    w = Workload(name, seed, num_layers, hq, hkv, d, KV_BF16, 0, ops)
+    fill, main = [], []
+    for i in range(n_chunks):
+        ops.append(("create", f"c{i}"))
+        w.kv_streams[f"cctx{i}"] = cctx[i] + chunk[i]
+        w.q_streams[f"cq{i}"] = chunk[i]
+        if cctx[i]:
+            fill.append((f"c{i}", cctx[i], [(f"cctx{i}", 0, cctx[i])], None, None))
+        main.append((f"c{i}", chunk[i], [(f"cctx{i}", cctx[i], chunk[i])], [(f"cq{i}", 0, chunk[i])], None))
+    for i in range(n_decode):
+        ops.append(("create", f"d{i}"))
+        w.kv_streams[f"dctx{i}"] = dctx[i] + 1
+        w.q_streams[f"dq{i}"] = 1
+        fill.append((f"d{i}", dctx[i], [(f"dctx{i}", 0, dctx[i])], None, None))
+        main.append((f"d{i}", 1, [(f"dctx{i}", dctx[i], 1)], [(f"dq{i}", 0, 1)], None))
+    ops.append(("pass", fill, False))
+    ops += [("freeze", f"c{i}", -1) for i in range(n_chunks)]
+    ops += [("freeze", f"d{i}", -1) for i in range(n_decode)]
+    ops.append(("pass", main, True))
+    w.num_pages = _pages_for([a + b for a, b in zip(cctx, chunk)]) + _pages_for([c + 1 for c in dctx]) + 32
+    w.chunks, w.chunk_ctx, w.decode_ctx = chunk, cctx, dctx
+    return w
+
+
+# The five workloads at full size (the parity tests also run reduced-size
+# variants of 2-5 that the oracle finishes in seconds).
+FULL = {
+    "tiny_decode": tiny_decode,
+    "llama8b_decode": llama8b_decode,
+    "fork_spec": fork_spec,
+    "mixed_batch": mixed_batch,
+    "llama70b_fp8": llama70b_fp8,
+}
+
+
+def reduced(name: str) -> Workload:
+    """Oracle-sized variant of a full workload: same structure and head shapes,
+    fewer working sets and shorter contexts, still several pages, splits and
+    MMA tiles long with ragged tails."""
+    if name == "tiny_decode":
+        return tiny_decode()
+    if name == "llama8b_decode":
+        return decode_batch(name="llama8b_decode_small", seed=12, n_ws=6, ctx_lo=200, ctx_hi=1500,
+                            num_layers=2)
+    if name == "fork_spec":
+        return fork_spec(name="fork_spec_small", seed=13, prompt=520, n_forks=5, suffix_hi=40)
+    if name == "mixed_batch":
+        return mixed_batch(name="mixed_batch_small", seed=14, n_chunks=3, chunk_lo=100, chunk_hi=300,
+                           ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400)
+    if name == "llama70b_fp8":
+        return decode_batch(name="llama70b_fp8_small", seed=15, n_ws=8, ctx_lo=300, ctx_hi=1200,
+                            num_layers=1, hq=64, hkv=8, d=128, kv_dtype=KV_E4M3,
+                            prefix_groups=2, prefix_len=160)
+    raise KeyError(name)
