@@ -1,0 +1,348 @@
+"""Benchmark of one batched decode pass over paged KV working sets.
+
+Workload (default): Llama-3.1-8B-shaped decode batch -- 64 working sets with
+contexts uniform in [512, 8192] (seeded), 32 query / 8 KV heads, head_dim 128,
+bf16 KV in 16-token pages, 32 layers of independent random K/V.  One step is
+one whole pass through the hot path: pie_batch_begin (slot reservation,
+plan, upload), then for each of the 32 layers pie_kv_append of the new
+token's K/V and pie_attend of its 32 query heads, pie_batch_end, and a
+rollback of the speculative token (host) so every step sees the same state.
+
+Metric: decode attend KV GB/s = algorithmic K/V bytes the attention reads
+(every valid key once per working set, K and V) / step time; plus query
+rows/s.  Inputs (KV cache, Q/K/V of the step) are resident in HBM; the KV
+read per layer (~1.1 GB) is far larger than L2, so no flush is needed.
+
+--impl reference times the CPU oracle instead (bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+        return float(hbm), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if len(r) > 8 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 8 and r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].strip() == "Active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def allmax(world, x):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_sample(w, seconds=12.0):
+    """Times the oracle's attention on a bounded sample of the workload: the
+    decode rows of the first working sets of one layer, as many as fit in
+    about `seconds`.  Returns (KV GB/s, rows/s, description, cores)."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import attention, kvstore
+
+    ctx = w.ctx
+    esize = 2 if w.kv_dtype == 0 else 1
+    rng = np.random.default_rng(0)
+    kv_bytes = rows = 0
+    elapsed = 0.0
+    used = []
+    for i, c in enumerate(ctx):
+        n = c + 1
+        st = kvstore.KVStore(1, w.num_q_heads, w.num_kv_heads, w.head_dim, -(-n // 16) + 1)
+        h = st.ws_create()
+        from paged_kv_attention_working_gb300.workloads import bf16_round
+
+        k = bf16_round(rng.standard_normal((n, w.num_kv_heads, w.head_dim), dtype=np.float32))
+        v = bf16_round(rng.standard_normal((n, w.num_kv_heads, w.head_dim), dtype=np.float32))
+        q = bf16_round(rng.standard_normal((1, w.num_q_heads, w.head_dim), dtype=np.float32))
+        p = st.begin([(h, n, None)])
+        st.kv_append(p, 0, k, v)
+        row_pass = kvstore.Pass([h], [n - 1], [p.rows_slot[-1]], [])
+        t0 = time.perf_counter()
+        attention.attend_pass(st, row_pass, 0, kvstore.bf16_bits_to_f64(q))
+        elapsed += time.perf_counter() - t0
+        kv_bytes += n * w.num_kv_heads * w.head_dim * esize * 2
+        rows += 1
+        used.append(c)
+        if elapsed > seconds:
+            break
+    cores = len(os.sched_getaffinity(0))
+    desc = (f"oracle attend_pass (float64 numpy, page gather + exact softmax) on {rows} decode rows "
+            f"(contexts {used[:4]}{'...' if len(used) > 4 else ''}) of one layer of the workload")
+    return kv_bytes / elapsed / 1e9, rows / elapsed, desc, cores, elapsed
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    per_step = []
+    gbs = rps = None
+    desc = cores = None
+    for i in range(args.warmup + args.steps):
+        gbs, rps, desc, cores, el = oracle_sample(w, seconds=args.ref_seconds)
+        if i >= args.warmup:
+            per_step.append(el)
+    line = {"impl": "reference", "metric": "decode attend KV GB/s", "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(per_step), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "n_ws": len(w.ctx), "layers": w.num_layers, "hq": w.num_q_heads,
+                       "hkv": w.num_kv_heads, "head_dim": w.head_dim, "kv_dtype": "bf16"},
+            "rows_per_s": rps,
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU leg
+def run_gpu(args, w, world, rank, local):
+    import torch
+
+    from paged_kv_attention_working_gb300 import pie
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    L, Hq, Hkv, D = w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim
+    esize = 2 if w.kv_dtype == 0 else 1
+    block = 16 * D * esize
+    pool_bytes = L * w.num_pages * Hkv * block
+    kpool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
+    vpool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
+    ks, vs = w.scales()
+    ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
+                             k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
+    names = [f"w{i}" for i in range(len(w.ctx))]
+    hs = {n: pie.pie_ws_create(ctx) for n in names}
+    # fill the contexts: one pass, random bf16 K/V per layer generated on the device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    b = pie.pie_batch_begin(ctx, [(hs[n], c, None) for n, c in zip(names, w.ctx)])
+    n_fill = pie.pie_batch_rows(b)
+    for layer in range(L):
+        k = torch.randn((n_fill, Hkv, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        v = torch.randn((n_fill, Hkv, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        pie.pie_kv_append(ctx, b, layer, k, v)
+        del k, v
+    pie.pie_batch_end(ctx, b)
+    for n in names:
+        pie.pie_ws_freeze(ctx, hs[n], -1)
+    torch.cuda.synchronize(dev)
+    n_rows = len(names)
+    q = torch.randn((L, n_rows, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
+    kn = torch.randn((L, n_rows, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    vn = torch.randn((L, n_rows, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty((L, n_rows, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((L, n_rows, Hq), dtype=torch.float32, device=dev)
+    segs = [(hs[n], 1, None) for n in names]
+
+    # algorithmic bytes of one attend launch (one layer): every visible key once
+    keys = sum(c + 1 for c in w.ctx)
+    pages = sum(-(-(c + 1) // 16) for c in w.ctx)
+    kv_bytes_layer = keys * Hkv * D * esize * 2
+    attend_bytes = kv_bytes_layer + 2 * n_rows * Hq * D * 2 + n_rows * Hq * 4 + 4 * pages
+    append_bytes = n_rows * Hkv * D * (2 + esize) * 2
+
+    info = {}
+
+    def step(ev=None, host=None):
+        if host is not None:
+            qh, kh, vh, oh = host
+            q.copy_(qh, non_blocking=True)
+            kn.copy_(kh, non_blocking=True)
+            vn.copy_(vh, non_blocking=True)
+        bb = pie.pie_batch_begin(ctx, segs)
+        info.update(pie.pie_batch_plan_info(bb))
+        for layer in range(L):
+            pie.pie_kv_append(ctx, bb, layer, kn[layer], vn[layer])
+            if ev is not None:
+                ev[layer][0].record(stream)
+            pie.pie_attend(ctx, bb, layer, q[layer], out[layer], lse[layer])
+            if ev is not None:
+                ev[layer][1].record(stream)
+        pie.pie_batch_end(ctx, bb)
+        if host is not None:
+            oh.copy_(out, non_blocking=True)
+        for n in names:
+            pie.pie_ws_rollback(ctx, hs[n], 1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pie.pie_ctx_check(ctx) == 0
+
+    # ---- device-resident timing
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(events[s])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+    ms = t0.elapsed_time(t1) / args.steps
+    ms = allmax(world, ms)
+    attend_ms = [e0.elapsed_time(e1) for st in events for e0, e1 in st]
+    attend_avg = statistics.mean(attend_ms)
+    assert pie.pie_ctx_check(ctx) == 0
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    host = (q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory(),
+            torch.empty(out.shape, dtype=out.dtype).pin_memory())
+    step(host=host)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        step(host=host)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = allmax(world, e0.elapsed_time(e1) / args.steps)
+    h2d = sum(t.numel() * t.element_size() for t in host[:3])
+    d2h = host[3].numel() * host[3].element_size()
+
+    hbm_peak, peak_src = peaks()
+    kv_step = kv_bytes_layer * L
+    value = world * kv_step / (ms * 1e-3) / 1e9
+    achieved = attend_bytes / (attend_avg * 1e-3) / 1e9
+    launches_per_layer = 1 + (info["decode_items"] > 0) + (info["prefill_items"] > 0) + (info["merge_rows"] > 0)
+    result = {
+        "metric": "decode attend KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "n_ws": n_rows, "contexts": "uniform [512, 8192] seeded", "layers": L,
+                   "hq": Hq, "hkv": Hkv, "head_dim": D, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
+                   "page_size": 16, "l2": "inputs larger than L2 (~1.1 GB KV per layer)",
+                   "parallelism": f"replicas x{world}"},
+        "rows_per_s": world * n_rows / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
+                     "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": attend_bytes, "avg_launch_ms": attend_avg},
+        "append": {"bytes_per_launch": append_bytes},
+        "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * L * launches_per_layer,
+        "clocks": clk,
+    }
+    pie.pie_ctx_destroy(ctx)
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from paged_kv_attention_working_gb300 import workloads as wl
+
+    w = wl.llama8b_decode()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        return
+    result = run_gpu(args, w, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            gbs, rps, desc, cores, _ = oracle_sample(w, seconds=args.ref_seconds)
+            result["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                      "sample": desc, "rows_per_s": rps}
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * pie_attn.h -- C ABI of a paged-KV attention library for GB300 (sm_103a).
+ *
+ * The library keeps the KV state of many working sets in a pool of 16-token
+ * pages and runs the per-layer attention step of a batched forward pass over
+ * them: ops.attn.kv_append followed by attend / prefill ("Poem ops",
+ * Operations table, row ops.attn).  Working sets follow "How Pie thinks",
+ * section 4 "Working sets": a frozen prefix of committed tokens plus a
+ * writable buffer of uncommitted (e.g. speculative) tokens; fork shares the
+ * frozen prefix without copying it; frozen pages are deduplicated across
+ * requests.  The runtime packs passes of many working sets into shared
+ * kernel launches ("How Pie thinks", "Batching is still the engine's job"):
+ * one pie_batch covers every segment of a pass, and one pie_kv_append /
+ * pie_attend call per layer covers every row of it.
+ *
+ * Conventions
+ *  - Every call returns a pie_status: 0 = PIE_OK, negative = error.  A
+ *    failed call changes no state; pie_last_error() then describes it.
+ *  - Handles are opaque.  A context is not thread-safe: one host thread at a
+ *    time.
+ *  - Device pointers passed in are owned by the caller and only borrowed for
+ *    stream-ordered use on the context's stream; no call synchronises that
+ *    stream except where stated (pie_ctx_destroy, buffer growth in
+ *    pie_batch_begin).
+ *  - All device work of a context runs on its stream, in call order.  The
+ *    caller must keep pools, inputs and outputs alive until that work ends.
+ *
+ * KV pool layout (device memory owned by the caller, borrowed by the
+ * context; K and V have separate pools of identical layout):
+ *    pool[layer][page][kv_head][block],
+ *    block = 16 * head_dim * esize bytes (esize 2 for bf16, 1 for e4m3).
+ *  A block is cut along the head dimension into panels of 128 bytes per key:
+ *  panel p holds bytes [p*128, p*128+128) of every key's head vector and
+ *  occupies block bytes [p*2048, p*2048+2048).  Within a panel, the 16-byte
+ *  chunk c of key slot s (s = position % 16) is stored at byte
+ *  s*128 + 16*(c ^ (s % 8)).  head_dim * esize must be a multiple of 128
+ *  (bf16: head_dim 64 or 128; e4m3: head_dim 128).  bf16 elements are their
+ *  little-endian bit patterns; e4m3 elements (OCP FP8 E4M3) are
+ *  round-to-nearest-even, saturating encodings of float32(x) * float32(1 /
+ *  scale[layer][kv_head]).
+ */
+#ifndef PIE_ATTN_H
+#define PIE_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pie_status;
+enum {
+  PIE_OK = 0,
+  PIE_ERR_INVALID = -1,    /* bad argument or configuration */
+  PIE_ERR_BAD_HANDLE = -2, /* unknown working set or batch */
+  PIE_ERR_NO_PAGES = -3,   /* the page pool cannot cover the pass */
+  PIE_ERR_RANGE = -4,      /* freeze / rollback beyond the writable buffer */
+  PIE_ERR_CUDA = -5,       /* a CUDA runtime call failed */
+  PIE_ERR_STATE = -6       /* call not allowed in the current state */
+};
+
+enum { PIE_KV_BF16 = 0, PIE_KV_E4M3 = 1 };
+
+typedef int32_t pie_ws;            /* working-set handle, > 0 */
+typedef struct pie_ctx pie_ctx;
+typedef struct pie_batch pie_batch;
+
+typedef struct pie_config {
+  int32_t num_layers;    /* layers sharing one page id space ("fold_layers") */
+  int32_t num_q_heads;   /* Hq */
+  int32_t num_kv_heads;  /* Hkv; Hq must be a multiple (grouped-query heads) */
+  int32_t head_dim;      /* d */
+  int32_t page_size;     /* must be 16 */
+  int32_t kv_dtype;      /* PIE_KV_BF16 or PIE_KV_E4M3 */
+  int32_t num_pages;     /* pages in each pool */
+  int32_t num_sms;       /* SMs to plan for; 0 = query the device (152 when
+                            k_pool is NULL) */
+  const int32_t* free_list; /* host, nullable, copied: initial order of the
+                               free-page stack, a permutation of
+                               0..num_pages-1, first entry allocated first;
+                               NULL = ascending */
+  const float* k_scale;  /* host, copied, [num_layers*num_kv_heads]; e4m3 only:
+                            dequantised K = code * k_scale[layer][kv_head] */
+  const float* v_scale;  /* likewise for V */
+  void* k_pool;          /* device, borrowed, layout above; NULL together with
+                            v_pool = plan-only context (host state only, no
+                            device work; pie_kv_append / pie_attend fail) */
+  void* v_pool;
+  void* stream;          /* cudaStream_t, borrowed; NULL = legacy default */
+} pie_config;
+
+/* One segment of a pass: n_new new tokens of working set ws.  token_ids
+ * (host, nullable, n_new entries) are recorded for prefix dedup; NULL means
+ * unknown, and pages holding unknown tokens are never deduplicated. */
+typedef struct pie_seg {
+  pie_ws ws;
+  int32_t n_new;
+  const int32_t* token_ids;
+} pie_seg;
+
+/* Context.  Copies the configuration, allocates small device buffers
+ * (scales, plan, partial results) with cudaMalloc when k_pool is set. */
+pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out);
+/* Synchronises the stream, frees everything the context allocated. */
+pie_status pie_ctx_destroy(pie_ctx* ctx);
+const char* pie_last_error(const pie_ctx* ctx);
+
+/* ---- working sets ("How Pie thinks", section 4; host state only) ----
+ * Not allowed while a batch is open (PIE_ERR_STATE). */
+
+/* New empty working set; handles count up from 1 and are never reused. */
+pie_status pie_ws_create(pie_ctx* ctx, pie_ws* out);
+/* Releases every page reference, highest logical page first. */
+pie_status pie_ws_destroy(pie_ctx* ctx, pie_ws ws);
+/* New working set holding the parent's frozen tokens only, sharing their
+ * pages (reference count + 1, no copy).  A shared partial page is copied
+ * lazily by the first pass that writes into it. */
+pie_status pie_ws_fork(pie_ctx* ctx, pie_ws parent, pie_ws* child);
+/* Commits the first n writable tokens (all when n < 0).  Pages that become
+ * fully frozen with known token ids are registered for dedup under
+ * (previous page, token ids) when the previous page is registered or this is
+ * page 0, unless that key is present.  n > writable: PIE_ERR_RANGE. */
+pie_status pie_ws_freeze(pie_ctx* ctx, pie_ws ws, int32_t n);
+/* Drops the last n writable tokens ("speculative drafts that you might roll
+ * back") and releases emptied pages, highest first.  n > writable:
+ * PIE_ERR_RANGE. */
+pie_status pie_ws_rollback(pie_ctx* ctx, pie_ws ws, int32_t n);
+/* Dedup lookup for an EMPTY working set: shares the registered pages whose
+ * token ids match token_ids[0..n) page by page from the start; the matched
+ * tokens become frozen.  *n_reused = matched tokens (a multiple of 16). */
+pie_status pie_ws_match_prefix(pie_ctx* ctx, pie_ws ws, const int32_t* token_ids,
+                               int32_t n, int32_t* n_reused);
+pie_status pie_ws_info(const pie_ctx* ctx, pie_ws ws, int32_t* n_tokens,
+                       int32_t* n_frozen, int32_t* n_pages);
+/* Copies up to cap physical page ids (logical order) into out; *n = count. */
+pie_status pie_ws_page_table(const pie_ctx* ctx, pie_ws ws, int32_t* out,
+                             int32_t cap, int32_t* n);
+pie_status pie_page_refcount(const pie_ctx* ctx, int32_t page, int32_t* rc);
+pie_status pie_free_pages(const pie_ctx* ctx, int32_t* n_free);
+
+/* ---- one batched pass ----
+ * Rows are the new tokens of all segments, in segment order, then token
+ * order.  Each working set may appear once.  Reserves a slot for every row
+ * (allocating pages segment by segment, token by token; a write into a
+ * shared page first copies it), builds the attention plan (per-row page
+ * tables and positions, fork/dedup groups, KV splits), uploads it with one
+ * host-to-device copy and enqueues the copy-on-write page copies on the
+ * stream.  The new tokens become writable tokens of their working sets.
+ * Fails with PIE_ERR_NO_PAGES, changing nothing, if the pool cannot cover
+ * the whole pass.  One batch may be open per context. */
+pie_status pie_batch_begin(pie_ctx* ctx, const pie_seg* segs, int32_t n_segs,
+                           pie_batch** out);
+/* Number of rows of the batch. */
+pie_status pie_batch_rows(const pie_batch* b, int32_t* n_rows);
+/* Host copies of the per-row position and slot (page * 16 + position % 16). */
+pie_status pie_batch_slots(const pie_batch* b, int32_t* pos, int32_t* slot);
+/* ops.attn.kv_append for one layer: k, v are device bf16 [n_rows][Hkv][d];
+ * row r is written to its reserved slot in the pool (converted to e4m3 for
+ * an e4m3 context). */
+pie_status pie_kv_append(pie_ctx* ctx, pie_batch* b, int32_t layer,
+                         const void* k, const void* v);
+/* ops.attn.attend / prefill for one layer: q device bf16 [n_rows][Hq][d];
+ * out device bf16 [n_rows][Hq][d]; lse device float [n_rows][Hq] (natural
+ * log of the softmax denominator) or NULL.  Row r at position p of working
+ * set w, query head h: softmax over keys 0..p of w, from KV head h / (Hq /
+ * Hkv), of (q . k) / sqrt(d), applied to the values.  Requires that
+ * pie_kv_append ran for this layer and batch first. */
+pie_status pie_attend(pie_ctx* ctx, pie_batch* b, int32_t layer,
+                      const void* q, void* out, float* lse);
+/* Closes the batch.  Its device work stays enqueued on the stream. */
+pie_status pie_batch_end(pie_ctx* ctx, pie_batch* b);
+
+/* ---- introspection (tests, tools) ---- */
+/* info[0..3] = decode-kernel items, tensor-core items, rows merged from
+ * several partial results, copy-on-write page copies. */
+pie_status pie_batch_plan_info(const pie_batch* b, int32_t* info);
+/* Copies work items (kind 0: decode kernel, 1: tensor-core kernel), 8 int32
+ * each: first page index into the batch's page list, pages, first key
+ * position, first row-list index, rows, part (-1 = direct output), keys,
+ * reserved.  *n = total items; at most cap are copied. */
+pie_status pie_batch_items(const pie_batch* b, int32_t kind, int32_t* out, int32_t cap,
+                           int32_t* n);
+/* Synchronises the stream and returns (and clears) the kernels' error bits:
+ * bit 0 = a bounded wait inside a kernel ran out (that launch's results are
+ * invalid).  0 = no error. */
+pie_status pie_ctx_check(pie_ctx* ctx, int32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PIE_ATTN_H */

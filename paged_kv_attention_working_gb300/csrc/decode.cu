@@ -1,0 +1,436 @@
+// Decode attention over paged KV ("Poem ops", ops.attn.attend) and the merge
+// of split / shared partial results.
+//
+// One CTA takes one work item for one KV head: up to 64 query rows x query
+// heads of that KV group (one decode token, a few speculative drafts, or the
+// rows of a small fork / dedup group) over a run of pages of one working set.
+// The item's pages stream through a ring of shared-memory stages, one 1-D
+// bulk async copy per K and per V page block (the pool's block layout is
+// already bank-conflict free for ldmatrix, see pie_attn.h), filled by a
+// producer warp.  Four consumer warps run QK^T and PV on the tensor cores
+// with warp-level m16n8k16 MMA (M = 16 query heads x rows, N = 8 keys or 8
+// head-dim columns) and keep an online softmax in registers.  When the item
+// has a single 16-row M tile the four warps take alternate pages and merge
+// their softmax states at the end; with 2 or 4 M tiles each warp owns a
+// tile and every page is read from HBM once for all of them, which is what
+// makes a fork group's shared pages cost one read per group ("How Pie
+// thinks", section 4: the prompt is computed once and shared).
+//
+// E4M3 pages are converted in registers to f16 scaled by 2^-8 (an exact bit
+// move) and the scales are folded into the softmax and output scaling.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace pie {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+template <bool E4M3, int D>
+struct DecodeCfg {
+  static constexpr int kEsize = E4M3 ? 1 : 2;
+  static constexpr int kBlock = kPageSize * D * kEsize;  // bytes per page-head block
+  static constexpr int kStages = E4M3 ? 12 : 8;
+  static constexpr int kStageBytes = 2 * kBlock;
+  static constexpr int kNT = D / 8;  // n-tiles of the output (head dim)
+  static constexpr int kKS = D / 16; // k-steps of QK^T
+  static constexpr int kCombineFloats = kConsumerWarps * 32 * (kNT * 4 + 4);
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kSmem = (kRing > kCombineFloats * 4 ? kRing : kCombineFloats * 4) + 2 * kStages * 8 + 16;
+};
+
+template <bool E4M3, int D>
+__global__ void __launch_bounds__(kThreads) decode_kernel(Geometry g, PlanView p, int layer,
+                                                          const __nv_bfloat16* __restrict__ q,
+                                                          const uint8_t* __restrict__ kpool,
+                                                          const uint8_t* __restrict__ vpool,
+                                                          const float* __restrict__ kscale,
+                                                          const float* __restrict__ vscale,
+                                                          __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                          float* __restrict__ part_acc, float* __restrict__ part_ml,
+                                                          int* err) {
+  using C = DecodeCfg<E4M3, D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (C::kSmem - 2 * C::kStages * 8 - 16));
+  uint64_t* empty = full + C::kStages;
+
+  const WorkItem it = p.dec_items[blockIdx.x];
+  const int head = blockIdx.y;
+  const int G = g.hq / g.hkv;
+  const int M = it.n_rows * G;
+  const int n_mt = M <= 16 ? 1 : (M <= 32 ? 2 : 4);
+  const int n_grp = kConsumerWarps / n_mt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t layer_blk = (static_cast<int64_t>(layer) * g.num_pages) * g.hkv;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], n_mt);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      bool ok = true;
+      for (int j = 0; j < it.n_pages; ++j) {
+        int s = j % C::kStages;
+        if (j >= C::kStages && ok) ok = mbar_wait(&empty[s], ((j / C::kStages) - 1) & 1, err);
+        if (!ok) break;
+        int page = p.page_ids[it.pages_off + j];
+        int64_t boff = (layer_blk + static_cast<int64_t>(page) * g.hkv + head) * C::kBlock;
+        uint8_t* st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kBlock);
+        bulk_g2s(st, kpool + boff, C::kBlock, &full[s]);
+        bulk_g2s(st + C::kBlock, vpool + boff, C::kBlock, &full[s]);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int mt = warp % n_mt, grp = warp / n_mt;
+  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group / thread in quad
+  const float kdq = E4M3 ? kscale[layer * g.hkv + head] * 256.0f : 1.0f;
+  const float vdq = E4M3 ? vscale[layer * g.hkv + head] * 256.0f : 1.0f;
+  const float qk_scale = kdq * rsqrtf(static_cast<float>(D)) * 1.4426950408889634f;
+
+  // the two M rows this thread holds: m = 16*mt + gq (+8)
+  int mrow[2], mpos[2];
+  const __nv_bfloat16* qptr[2];
+  for (int h = 0; h < 2; ++h) {
+    int m = 16 * mt + gq + 8 * h;
+    mrow[h] = -1;
+    mpos[h] = -1;
+    qptr[h] = nullptr;
+    if (m < M) {
+      int rl = m / G, hl = m % G;
+      int row = p.row_list[it.rows_off + rl];
+      mrow[h] = row;
+      mpos[h] = p.row_pos[row];
+      qptr[h] = q + (static_cast<int64_t>(row) * g.hq + head * G + hl) * D;
+    }
+  }
+  // Q as A fragments: qa[ks][0..3] = (row g, k 2t..) (row g+8, k 2t..) (row g, k 2t+8..) (row g+8, k 2t+8..)
+  uint32_t qa[C::kKS][4];
+#pragma unroll
+  for (int ks = 0; ks < C::kKS; ++ks) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t lo = 0, hi = 0;
+      if (qptr[h]) {
+        if constexpr (!E4M3) {
+          lo = *reinterpret_cast<const uint32_t*>(qptr[h] + 16 * ks + 2 * tq);
+          hi = *reinterpret_cast<const uint32_t*>(qptr[h] + 16 * ks + 8 + 2 * tq);
+        } else {
+          // k-slots 2t,2t+1 <-> d 16ks+4t, +1 ; 2t+8,2t+9 <-> d 16ks+4t+2, +3
+          uint2 w = *reinterpret_cast<const uint2*>(qptr[h] + 16 * ks + 4 * tq);
+          float f0 = __uint_as_float(w.x << 16), f1 = __uint_as_float(w.x & 0xFFFF0000u);
+          float f2 = __uint_as_float(w.y << 16), f3 = __uint_as_float(w.y & 0xFFFF0000u);
+          lo = pack_f16(f0, f1);
+          hi = pack_f16(f2, f3);
+        }
+      }
+      qa[ks][h] = lo;
+      qa[ks][2 + h] = hi;
+    }
+  }
+
+  float o[C::kNT][4];
+#pragma unroll
+  for (int i = 0; i < C::kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mx[2] = {-INFINITY, -INFINITY}, sum[2] = {0.f, 0.f};
+  bool ok = true;
+
+  for (int j = grp; j < it.n_pages; j += n_grp) {
+    const int s = j % C::kStages;
+    if (ok) ok = mbar_wait(&full[s], (j / C::kStages) & 1, err);
+    if (!ok) break;
+    const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
+    const uint32_t vb = kb + C::kBlock;
+
+    // ---- S = Q K^T for 16 keys: two n-tiles of 8 keys
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (!E4M3) {
+      const int key = (lane & 7) + ((lane >> 4) << 3);
+      const int csel = (lane >> 3) & 1;
+#pragma unroll
+      for (int ks = 0; ks < C::kKS; ++ks) {
+        int panel = ks >> 2, c = 2 * (ks & 3) + csel;
+        uint32_t addr = kb + panel * 2048 + key * 128 + 16 * (c ^ (key & 7));
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(addr, b0, b1, b2, b3);
+        mma16816<true>(sc[0], qa[ks], b0, b1);
+        mma16816<true>(sc[1], qa[ks], b2, b3);
+      }
+    } else {
+      const int key = (lane & 7) + ((lane >> 4) << 3);
+      const int csel = (lane >> 3) & 1;
+#pragma unroll
+      for (int kp = 0; kp < C::kKS / 2; ++kp) {
+        int c = 2 * kp + csel;
+        uint32_t addr = kb + key * 128 + 16 * (c ^ (key & 7));
+        uint32_t r0, r1, r2, r3;  // (keys 0-7, chunk 2kp) (0-7, 2kp+1) (8-15, 2kp) (8-15, 2kp+1)
+        ldsm_x4(addr, r0, r1, r2, r3);
+        mma16816<false>(sc[0], qa[2 * kp], e4m3x2_to_f16x2_scaled(prmt(r0, 0, 0x1404)),
+                        e4m3x2_to_f16x2_scaled(prmt(r0, 0, 0x3424)));
+        mma16816<false>(sc[1], qa[2 * kp], e4m3x2_to_f16x2_scaled(prmt(r2, 0, 0x1404)),
+                        e4m3x2_to_f16x2_scaled(prmt(r2, 0, 0x3424)));
+        mma16816<false>(sc[0], qa[2 * kp + 1], e4m3x2_to_f16x2_scaled(prmt(r1, 0, 0x1404)),
+                        e4m3x2_to_f16x2_scaled(prmt(r1, 0, 0x3424)));
+        mma16816<false>(sc[1], qa[2 * kp + 1], e4m3x2_to_f16x2_scaled(prmt(r3, 0, 0x1404)),
+                        e4m3x2_to_f16x2_scaled(prmt(r3, 0, 0x3424)));
+      }
+    }
+
+    // ---- mask, online softmax (log2 domain)
+    const int kbase = it.key_base + 16 * j;
+    float pm[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float best = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          int kpos = kbase + nt * 8 + 2 * tq + e;
+          float v = kpos <= mpos[h] ? sc[nt][2 * h + e] * qk_scale : -INFINITY;
+          sc[nt][2 * h + e] = v;
+          best = fmaxf(best, v);
+        }
+      best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
+      best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
+      float mnew = fmaxf(mx[h], best);
+      float base = mnew == -INFINITY ? 0.f : mnew;
+      float alpha = ex2(mx[h] - base);
+      mx[h] = mnew;
+      pm[h] = base;
+      sum[h] *= alpha;
+#pragma unroll
+      for (int i = 0; i < C::kNT; ++i) {
+        o[i][2 * h] *= alpha;
+        o[i][2 * h + 1] *= alpha;
+      }
+    }
+    uint32_t pa[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float e0 = ex2(sc[nt][2 * h] - pm[h]), e1 = ex2(sc[nt][2 * h + 1] - pm[h]);
+        sum[h] += e0 + e1;
+        pa[2 * nt + h] = E4M3 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+      }
+
+    // ---- O += P V
+    if constexpr (!E4M3) {
+      const int key = (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int csel = lane >> 4;
+#pragma unroll
+      for (int np = 0; np < C::kNT / 2; ++np) {
+        int cc = 2 * np + csel;  // 16-byte d chunk (8 columns)
+        int panel = cc >> 3, c = cc & 7;
+        uint32_t addr = vb + panel * 2048 + key * 128 + 16 * (c ^ (key & 7));
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(addr, b0, b1, b2, b3);
+        mma16816<true>(o[2 * np], pa, b0, b1);
+        mma16816<true>(o[2 * np + 1], pa, b2, b3);
+      }
+    } else {
+#pragma unroll
+      for (int mq = 0; mq < D / 32; ++mq) {
+        uint32_t w[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          int key = 2 * tq + (jj & 1) + ((jj >> 1) << 3);
+          int c = 2 * mq + (gq >> 2);
+          w[jj] = lds32(vb + key * 128 + 16 * (c ^ (key & 7)) + 4 * (gq & 3));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t sel = i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12);
+          uint32_t b0 = e4m3x2_to_f16x2_scaled(prmt(w[0], w[1], sel));
+          uint32_t b1 = e4m3x2_to_f16x2_scaled(prmt(w[2], w[3], sel));
+          mma16816<false>(o[4 * mq + i], pa, b0, b1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ---- finish: quad sums, then merge warps that shared an M tile
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
+    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
+  }
+  if (n_grp > 1) {
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32));
+    float* cm = reinterpret_cast<float*>(smem);
+    const int stride = C::kNT * 4 + 4;
+    float* mine = cm + (warp * 32 + lane) * stride;
+    if (grp > 0) {
+#pragma unroll
+      for (int i = 0; i < C::kNT; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mine[i * 4 + e] = o[i][e];
+      mine[C::kNT * 4 + 0] = mx[0];
+      mine[C::kNT * 4 + 1] = mx[1];
+      mine[C::kNT * 4 + 2] = sum[0];
+      mine[C::kNT * 4 + 3] = sum[1];
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32));
+    if (grp > 0) return;
+    for (int og = 1; og < n_grp; ++og) {
+      const float* th = cm + ((og * n_mt + mt) * 32 + lane) * stride;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float m2 = th[C::kNT * 4 + h], l2 = th[C::kNT * 4 + 2 + h];
+        float mnew = fmaxf(mx[h], m2);
+        float base = mnew == -INFINITY ? 0.f : mnew;
+        float a1 = ex2(mx[h] - base), a2 = ex2(m2 - base);
+        sum[h] = sum[h] * a1 + l2 * a2;
+        mx[h] = mnew;
+#pragma unroll
+        for (int i = 0; i < C::kNT; ++i) {
+          o[i][2 * h] = o[i][2 * h] * a1 + th[i * 4 + 2 * h] * a2;
+          o[i][2 * h + 1] = o[i][2 * h + 1] * a1 + th[i * 4 + 2 * h + 1] * a2;
+        }
+      }
+    }
+  }
+
+  // ---- write: direct bf16 output, or fp32 partial (acc, m, l) for merging
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (mrow[h] < 0) continue;
+    int m = 16 * mt + gq + 8 * h;
+    int qh = head * G + m % G;
+    int row = mrow[h];
+    if (it.part < 0) {
+      float inv = sum[h] > 0.f ? vdq / sum[h] : 0.f;
+      __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D;
+#pragma unroll
+      for (int i = 0; i < C::kNT; ++i) {
+        if constexpr (!E4M3) {
+          *reinterpret_cast<uint32_t*>(dst + 8 * i + 2 * tq) =
+              pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+        } else {
+          int mq = i >> 2, ii = i & 3;
+          dst[32 * mq + 8 * tq + ii] = __float2bfloat16_rn(o[i][2 * h] * inv);
+          dst[32 * mq + 8 * tq + 4 + ii] = __float2bfloat16_rn(o[i][2 * h + 1] * inv);
+        }
+      }
+      if (lse && tq == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (mx[h] + __log2f(sum[h])) * 0.6931471805599453f;
+    } else {
+      int64_t slot = static_cast<int64_t>(p.row_part_base[row] + it.part) * g.hq + qh;
+      float* dst = part_acc + slot * D;
+#pragma unroll
+      for (int i = 0; i < C::kNT; ++i) {
+        if constexpr (!E4M3) {
+          *reinterpret_cast<float2*>(dst + 8 * i + 2 * tq) = make_float2(o[i][2 * h] * vdq, o[i][2 * h + 1] * vdq);
+        } else {
+          int mq = i >> 2, ii = i & 3;
+          dst[32 * mq + 8 * tq + ii] = o[i][2 * h] * vdq;
+          dst[32 * mq + 8 * tq + 4 + ii] = o[i][2 * h + 1] * vdq;
+        }
+      }
+      if (tq == 0) *reinterpret_cast<float2*>(part_ml + slot * 2) = make_float2(mx[h], sum[h]);
+    }
+  }
+}
+
+// One warp per (merged row, query head): combine the row's parts
+// (m_i, l_i, acc_i) in the log2 domain:
+//   m = max m_i,  l = sum l_i 2^(m_i - m),  o = sum acc_i 2^(m_i - m) / l.
+template <int D>
+__global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                             const float* __restrict__ part_acc, const float* __restrict__ part_ml) {
+  int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= p.n_merge * g.hq) return;
+  int i = wid / g.hq, qh = wid % g.hq;
+  int row = p.merge_rows[i], np = p.merge_nparts[i], base = p.row_part_base[row];
+  float m = -INFINITY;
+  for (int k = 0; k < np; ++k) m = fmaxf(m, part_ml[(static_cast<int64_t>(base + k) * g.hq + qh) * 2]);
+  float base_m = m == -INFINITY ? 0.f : m;
+  constexpr int E = D / 32;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float l = 0.f;
+  for (int k = 0; k < np; ++k) {
+    int64_t slot = static_cast<int64_t>(base + k) * g.hq + qh;
+    float2 ml = *reinterpret_cast<const float2*>(part_ml + slot * 2);
+    float w = ex2(ml.x - base_m);
+    l += ml.y * w;
+    const float* a = part_acc + slot * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += a[lane * E + e] * w;
+  }
+  float inv = l > 0.f ? 1.f / l : 0.f;
+  __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
+  if (lse && lane == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (m + __log2f(l)) * 0.6931471805599453f;
+}
+
+template <bool E4M3, int D>
+cudaError_t launch_decode_t(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
+                            const void* vpool, const float* ks, const float* vs, void* out, float* lse,
+                            float* acc, float* ml, int* err, cudaStream_t st) {
+  using C = DecodeCfg<E4M3, D>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<E4M3, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  dim3 grid(p.n_dec, g.hkv);
+  decode_kernel<E4M3, D><<<grid, kThreads, C::kSmem, st>>>(
+      g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
+      static_cast<const uint8_t*>(vpool), ks, vs, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
+                          const void* vpool, const float* scale_k, const float* scale_v, void* out, float* lse,
+                          float* part_acc, float* part_ml, int* err, cudaStream_t st) {
+  if (p.n_dec == 0) return cudaSuccess;
+  if (g.kv_dtype == 0 && g.d == 128)
+    return launch_decode_t<false, 128>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml,
+                                       err, st);
+  if (g.kv_dtype == 0 && g.d == 64)
+    return launch_decode_t<false, 64>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml,
+                                      err, st);
+  if (g.kv_dtype == 1 && g.d == 128)
+    return launch_decode_t<true, 128>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml,
+                                      err, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float* lse, const float* part_acc,
+                         const float* part_ml, cudaStream_t st) {
+  if (p.n_merge == 0) return cudaSuccess;
+  int64_t warps = static_cast<int64_t>(p.n_merge) * g.hq;
+  unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+  if (g.d == 128)
+    merge_kernel<128><<<blocks, 256, 0, st>>>(g, p, static_cast<__nv_bfloat16*>(out), lse, part_acc, part_ml);
+  else
+    merge_kernel<64><<<blocks, 256, 0, st>>>(g, p, static_cast<__nv_bfloat16*>(out), lse, part_acc, part_ml);
+  return cudaGetLastError();
+}
+
+}  // namespace pie

@@ -1,0 +1,821 @@
+// Host core of the paged-KV attention library: page allocator, reference
+// counts, prefix dedup table, working-set state machine, per-pass slot
+// reservation and attention planner, and the C ABI declared in pie_attn.h.
+//
+// Working-set semantics follow "How Pie thinks", section 4 "Working sets"
+// (frozen prefix, writable buffer, fork without copying, dedup of frozen
+// pages across requests); the per-pass planning step is the runtime's
+// packing of many passes into shared launches ("How Pie thinks", "Batching
+// is still the engine's job") and the role of ops.attn.plan_prefill ("Poem
+// ops", Operations table).
+#include <algorithm>
+#include <array>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pie_attn.h"
+#include "plan.h"
+
+using pie::CopyItem;
+using pie::kPageSize;
+using pie::WorkItem;
+
+namespace {
+
+// Rows x query-heads per item above which the tensor-core kernel takes the
+// item (it tiles 256 of them per CTA); the decode kernel takes up to 64.
+constexpr int kDecodeMaxM = 64;
+constexpr int kPrefillTileM = 256;
+constexpr int kMinSplitPages = 16;
+
+struct DedupKey {
+  std::array<int32_t, kPageSize + 1> v;  // predecessor page (-1 at page 0), token ids
+  bool operator==(const DedupKey& o) const { return v == o.v; }
+};
+struct DedupHash {
+  size_t operator()(const DedupKey& k) const {
+    uint64_t h = 0x9E3779B97F4A7C15ull;
+    for (int32_t x : k.v) {
+      h ^= static_cast<uint32_t>(x);
+      h *= 0xBF58476D1CE4E5B9ull;
+      h ^= h >> 31;
+    }
+    return static_cast<size_t>(h);
+  }
+};
+
+struct WorkingSet {
+  std::vector<int32_t> tokens;  // token ids, -1 = unknown
+  int32_t n_frozen = 0;
+  std::vector<int32_t> pages;
+  int32_t n_tokens() const { return static_cast<int32_t>(tokens.size()); }
+};
+
+inline int32_t cdiv(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
+
+}  // namespace
+
+struct pie_batch {
+  pie_ctx* ctx = nullptr;
+  int32_t n_rows = 0;
+  std::vector<int32_t> row_pos, row_slot;
+  std::vector<WorkItem> dec, pre;  // host copies of the work items
+  pie::PlanView view{};
+  bool appended_any = false;
+};
+
+struct pie_ctx {
+  pie_config cfg{};
+  pie::Geometry geo{};
+  int32_t num_sms = 152;
+  bool plan_only = true;
+  cudaStream_t stream = nullptr;
+  std::string err;
+
+  std::vector<int32_t> free_stack;  // back() = next page to allocate
+  std::vector<int32_t> refcount;
+  std::unordered_map<DedupKey, int32_t, DedupHash> dedup;
+  std::unordered_map<int32_t, DedupKey> page_key;
+  std::unordered_map<int32_t, WorkingSet> ws;
+  int32_t next_ws = 1;
+  std::vector<float> k_scale, v_scale;
+
+  // device buffers owned by the context
+  float* d_scales = nullptr;  // [4][L*Hkv]: k_scale, v_scale, 1/k_scale, 1/v_scale
+  int* d_err = nullptr;       // error bits set by kernels (bounded waits that ran out)
+  uint8_t* d_plan = nullptr;
+  size_t plan_cap = 0;
+  uint8_t* h_plan = nullptr;  // pinned staging
+  size_t h_plan_cap = 0;
+  cudaEvent_t upload_done = nullptr;
+  bool upload_pending = false;
+  float* d_part = nullptr;  // partial (acc | m,l) results
+  size_t part_cap = 0;      // floats
+  pie_batch* open = nullptr;
+};
+
+namespace {
+
+pie_status fail(pie_ctx* c, pie_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf;
+  return st;
+}
+
+pie_status cuda_fail(pie_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, PIE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+WorkingSet* find_ws(pie_ctx* c, pie_ws h) {
+  auto it = c->ws.find(h);
+  return it == c->ws.end() ? nullptr : &it->second;
+}
+
+int32_t alloc_page(pie_ctx* c) {
+  int32_t p = c->free_stack.back();
+  c->free_stack.pop_back();
+  c->refcount[p] = 1;
+  return p;
+}
+
+void release_page(pie_ctx* c, int32_t p) {
+  if (--c->refcount[p] == 0) {
+    auto it = c->page_key.find(p);
+    if (it != c->page_key.end()) {
+      c->dedup.erase(it->second);
+      c->page_key.erase(it);
+    }
+    c->free_stack.push_back(p);
+  }
+}
+
+void release_from(pie_ctx* c, WorkingSet& w, size_t keep) {
+  while (w.pages.size() > keep) {
+    int32_t p = w.pages.back();
+    w.pages.pop_back();
+    release_page(c, p);
+  }
+}
+
+// Grow a device buffer; the stream is synchronised first because work still
+// queued may read the old buffer.
+template <class T>
+pie_status ensure_device(pie_ctx* c, T** buf, size_t* cap, size_t need) {
+  if (need <= *cap) return PIE_OK;
+  size_t n = std::max(need, *cap + *cap / 2);
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaStreamSynchronize");
+  if (*buf) cudaFree(*buf);
+  *buf = nullptr;
+  *cap = 0;
+  e = cudaMalloc(reinterpret_cast<void**>(buf), n * sizeof(T));
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaMalloc");
+  *cap = n;
+  return PIE_OK;
+}
+
+// -------------------------------------------------------------- planner
+struct PlanBuilder {
+  std::vector<int32_t> page_ids, row_pos, row_slot, row_part_base, row_list;
+  std::vector<int32_t> merge_rows, merge_nparts;
+  std::vector<CopyItem> copies;
+  std::vector<WorkItem> dec, pre;
+};
+
+struct SegInfo {
+  int32_t seg, n0, n_new, row0, table_off, n_pages, shared_pages, group;
+};
+
+void split_pages(int32_t n_pages, int32_t chunk, std::vector<std::pair<int32_t, int32_t>>& out) {
+  out.clear();
+  if (n_pages <= 0) return;
+  int32_t n = std::max(1, cdiv(n_pages, chunk));
+  for (int32_t i = 0; i < n; ++i) {
+    int32_t a = static_cast<int32_t>(static_cast<int64_t>(n_pages) * i / n);
+    int32_t b = static_cast<int32_t>(static_cast<int64_t>(n_pages) * (i + 1) / n);
+    if (b > a) out.push_back({a, b - a});
+  }
+}
+
+void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows, PlanBuilder& pb) {
+  const int32_t G = c->geo.hq / c->geo.hkv;
+  std::vector<SegInfo> segs = segs_in;
+  // fork / dedup groups: segments whose tables start with the same page
+  std::unordered_map<int32_t, std::vector<int32_t>> by_first;
+  std::vector<int32_t> first_order;
+  for (size_t i = 0; i < segs.size(); ++i) {
+    int32_t p0 = pb.page_ids[segs[i].table_off];
+    auto& v = by_first[p0];
+    if (v.empty()) first_order.push_back(p0);
+    v.push_back(static_cast<int32_t>(i));
+  }
+  struct Group {
+    std::vector<int32_t> members;
+    int32_t cp;
+  };
+  std::vector<Group> groups;
+  for (int32_t p0 : first_order) {
+    auto& m = by_first[p0];
+    if (m.size() < 2) continue;
+    int32_t cp = INT32_MAX;
+    for (int32_t i : m) cp = std::min(cp, segs[i].n0 / kPageSize);
+    const int32_t* t0 = &pb.page_ids[segs[m[0]].table_off];
+    for (int32_t j = 0; j < cp; ++j)
+      for (int32_t i : m)
+        if (pb.page_ids[segs[i].table_off + j] != t0[j]) {
+          cp = j;
+          break;
+        }
+    if (cp <= 0) continue;
+    for (int32_t i : m) {
+      segs[i].shared_pages = cp;
+      segs[i].group = static_cast<int32_t>(groups.size());
+    }
+    groups.push_back({m, cp});
+  }
+
+  // pages of decode-kernel work, to size the KV splits
+  int64_t dec_pages = 0;
+  for (auto& g : groups) {
+    int32_t rows = 0;
+    for (int32_t i : g.members) rows += segs[i].n_new;
+    if (static_cast<int64_t>(rows) * G <= kDecodeMaxM) dec_pages += g.cp;
+  }
+  for (auto& s : segs)
+    if (static_cast<int64_t>(s.n_new) * G <= kDecodeMaxM) dec_pages += s.n_pages - s.shared_pages;
+  int64_t target_items = std::max<int64_t>(1, static_cast<int64_t>(c->num_sms) * 8 / c->geo.hkv);
+  int32_t chunk = static_cast<int32_t>(std::max<int64_t>(kMinSplitPages, (dec_pages + target_items - 1) / target_items));
+
+  std::vector<int32_t> n_parts(n_rows, 0);
+  struct Pending {
+    WorkItem it;
+    bool decode;
+  };
+  std::vector<Pending> items;
+  std::vector<std::pair<int32_t, int32_t>> sp;
+
+  // shared items first: part indices 0..k-1 of every member row
+  std::vector<int32_t> group_parts(groups.size(), 0);
+  for (size_t gi = 0; gi < groups.size(); ++gi) {
+    auto& g = groups[gi];
+    int32_t rows_off = static_cast<int32_t>(pb.row_list.size());
+    for (int32_t i : g.members)
+      for (int32_t r = 0; r < segs[i].n_new; ++r) pb.row_list.push_back(segs[i].row0 + r);
+    int32_t rows = static_cast<int32_t>(pb.row_list.size()) - rows_off;
+    const SegInfo& s0 = segs[g.members[0]];
+    bool decode = static_cast<int64_t>(rows) * G <= kDecodeMaxM;
+    int32_t kv_chunk = chunk;
+    if (!decode) {
+      // tensor-core items: tile the rows by 256 query heads, split the keys
+      // so the group fills the GPU (each page still read once per row tile)
+      int32_t tiles = cdiv(static_cast<int64_t>(rows) * G, kPrefillTileM);
+      int64_t want = std::max<int64_t>(1, static_cast<int64_t>(c->num_sms) / (c->geo.hkv * tiles));
+      kv_chunk = std::max<int32_t>(8, cdiv(g.cp, want));
+    }
+    split_pages(g.cp, kv_chunk, sp);
+    int32_t rt_rows = decode ? rows : std::max(1, kPrefillTileM / G);
+    for (int32_t r0 = 0; r0 < rows; r0 += rt_rows) {
+      int32_t nr = std::min(rt_rows, rows - r0);
+      for (size_t j = 0; j < sp.size(); ++j) {
+        WorkItem it{};
+        it.pages_off = s0.table_off + sp[j].first;
+        it.n_pages = sp[j].second;
+        it.key_base = sp[j].first * kPageSize;
+        it.n_keys = sp[j].second * kPageSize;
+        it.rows_off = rows_off + r0;
+        it.n_rows = nr;
+        it.part = static_cast<int32_t>(j);
+        items.push_back({it, decode});
+      }
+    }
+    group_parts[gi] = static_cast<int32_t>(sp.size());
+    for (int32_t i : g.members)
+      for (int32_t r = 0; r < segs[i].n_new; ++r) n_parts[segs[i].row0 + r] += static_cast<int32_t>(sp.size());
+  }
+
+  // private items of each segment
+  for (auto& s : segs) {
+    int32_t base_part = s.group >= 0 ? group_parts[s.group] : 0;
+    int32_t priv = s.n_pages - s.shared_pages;
+    if (static_cast<int64_t>(s.n_new) * G <= kDecodeMaxM) {
+      split_pages(priv, chunk, sp);
+      for (size_t j = 0; j < sp.size(); ++j) {
+        WorkItem it{};
+        int32_t first = s.shared_pages + sp[j].first;
+        it.pages_off = s.table_off + first;
+        it.n_pages = sp[j].second;
+        it.key_base = first * kPageSize;
+        it.n_keys = std::min(sp[j].second * kPageSize, s.n0 + s.n_new - it.key_base);
+        it.rows_off = s.row0;  // row_list[0..n_rows) is the identity
+        it.n_rows = s.n_new;
+        it.part = base_part + static_cast<int32_t>(j);
+        items.push_back({it, true});
+      }
+      for (int32_t r = 0; r < s.n_new; ++r) n_parts[s.row0 + r] += static_cast<int32_t>(sp.size());
+    } else {
+      int32_t rt_rows = std::max(1, kPrefillTileM / G);
+      for (int32_t r0 = 0; r0 < s.n_new; r0 += rt_rows) {
+        int32_t nr = std::min(rt_rows, s.n_new - r0);
+        int32_t last_pos = s.n0 + r0 + nr - 1;
+        WorkItem it{};
+        it.pages_off = s.table_off + s.shared_pages;
+        it.key_base = s.shared_pages * kPageSize;
+        it.n_pages = cdiv(last_pos + 1, kPageSize) - s.shared_pages;
+        it.n_keys = last_pos + 1 - it.key_base;
+        it.rows_off = s.row0 + r0;
+        it.n_rows = nr;
+        it.part = base_part;
+        items.push_back({it, false});
+        for (int32_t r = 0; r < nr; ++r) n_parts[s.row0 + r0 + r] += 1;
+      }
+    }
+  }
+
+  // part bases: rows with a single part are written directly
+  int32_t total = 0;
+  pb.row_part_base.assign(n_rows, -1);
+  for (int32_t r = 0; r < n_rows; ++r) {
+    if (n_parts[r] >= 2) {
+      pb.row_part_base[r] = total;
+      total += n_parts[r];
+      pb.merge_rows.push_back(r);
+      pb.merge_nparts.push_back(n_parts[r]);
+    }
+  }
+  for (auto& p : items) {
+    int32_t r0 = pb.row_list[p.it.rows_off];
+    if (n_parts[r0] < 2) p.it.part = -1;
+    (p.decode ? pb.dec : pb.pre).push_back(p.it);
+  }
+  // longest first, so the tail of each launch is made of short items
+  auto longer = [](const WorkItem& a, const WorkItem& b) {
+    int64_t ca = static_cast<int64_t>(a.n_pages) * a.n_rows, cb = static_cast<int64_t>(b.n_pages) * b.n_rows;
+    if (ca != cb) return ca > cb;
+    return a.pages_off < b.pages_off;
+  };
+  std::stable_sort(pb.dec.begin(), pb.dec.end(), [](const WorkItem& a, const WorkItem& b) {
+    return a.n_pages > b.n_pages;
+  });
+  std::stable_sort(pb.pre.begin(), pb.pre.end(), longer);
+}
+
+template <class T>
+size_t put(std::vector<uint8_t>& blob, const std::vector<T>& v, size_t align = 16) {
+  size_t off = (blob.size() + align - 1) / align * align;
+  blob.resize(off + v.size() * sizeof(T));
+  if (!v.empty()) std::memcpy(blob.data() + off, v.data(), v.size() * sizeof(T));
+  return off;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* pie_last_error(const pie_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out) {
+  if (!cfg || !out) return PIE_ERR_INVALID;
+  *out = nullptr;
+  const pie_config& k = *cfg;
+  int esize = k.kv_dtype == PIE_KV_BF16 ? 2 : (k.kv_dtype == PIE_KV_E4M3 ? 1 : 0);
+  if (k.num_layers <= 0 || k.num_q_heads <= 0 || k.num_kv_heads <= 0 || k.num_pages <= 0 || esize == 0 ||
+      k.page_size != kPageSize || k.num_q_heads % k.num_kv_heads)
+    return PIE_ERR_INVALID;
+  int G = k.num_q_heads / k.num_kv_heads;
+  bool dim_ok = (k.kv_dtype == PIE_KV_BF16 && (k.head_dim == 64 || k.head_dim == 128)) ||
+                (k.kv_dtype == PIE_KV_E4M3 && k.head_dim == 128);
+  if (!dim_ok || G > 64 || (G & (G - 1))) return PIE_ERR_INVALID;
+  if ((k.k_pool == nullptr) != (k.v_pool == nullptr)) return PIE_ERR_INVALID;
+  if (k.kv_dtype == PIE_KV_E4M3 && (!k.k_scale || !k.v_scale)) return PIE_ERR_INVALID;
+
+  auto* c = new pie_ctx();
+  c->cfg = k;
+  c->geo = {k.num_layers, k.num_q_heads, k.num_kv_heads, k.head_dim, k.num_pages, k.kv_dtype,
+            static_cast<int64_t>(kPageSize) * k.head_dim * esize};
+  c->plan_only = k.k_pool == nullptr;
+  c->stream = static_cast<cudaStream_t>(k.stream);
+  c->refcount.assign(k.num_pages, 0);
+  c->free_stack.resize(k.num_pages);
+  if (k.free_list) {
+    std::vector<char> seen(k.num_pages, 0);
+    for (int32_t i = 0; i < k.num_pages; ++i) {
+      int32_t p = k.free_list[i];
+      if (p < 0 || p >= k.num_pages || seen[p]) {
+        delete c;
+        return PIE_ERR_INVALID;
+      }
+      seen[p] = 1;
+      c->free_stack[k.num_pages - 1 - i] = p;
+    }
+  } else {
+    for (int32_t i = 0; i < k.num_pages; ++i) c->free_stack[k.num_pages - 1 - i] = i;
+  }
+  const int32_t nsc = k.num_layers * k.num_kv_heads;
+  c->k_scale.assign(nsc, 1.0f);
+  c->v_scale.assign(nsc, 1.0f);
+  if (k.kv_dtype == PIE_KV_E4M3) {
+    for (int32_t i = 0; i < nsc; ++i) {
+      if (!(k.k_scale[i] > 0.0f) || !(k.v_scale[i] > 0.0f)) {
+        delete c;
+        return PIE_ERR_INVALID;
+      }
+      c->k_scale[i] = k.k_scale[i];
+      c->v_scale[i] = k.v_scale[i];
+    }
+  }
+  c->cfg.free_list = nullptr;
+  c->cfg.k_scale = c->cfg.v_scale = nullptr;
+  c->num_sms = k.num_sms > 0 ? k.num_sms : 152;
+  if (!c->plan_only) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && k.num_sms <= 0) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    std::vector<float> sc(4 * nsc);
+    for (int32_t i = 0; i < nsc; ++i) {
+      sc[i] = c->k_scale[i];
+      sc[nsc + i] = c->v_scale[i];
+      sc[2 * nsc + i] = 1.0f / c->k_scale[i];
+      sc[3 * nsc + i] = 1.0f / c->v_scale[i];
+    }
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&c->d_scales), sc.size() * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemcpy(c->d_scales, sc.data(), sc.size() * sizeof(float), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&c->d_err), sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      pie_ctx_destroy(c);
+      return PIE_ERR_CUDA;
+    }
+  }
+  *out = c;
+  return PIE_OK;
+}
+
+pie_status pie_ctx_destroy(pie_ctx* c) {
+  if (!c) return PIE_ERR_INVALID;
+  if (!c->plan_only) {
+    cudaStreamSynchronize(c->stream);
+    if (c->d_scales) cudaFree(c->d_scales);
+    if (c->d_err) cudaFree(c->d_err);
+    if (c->d_plan) cudaFree(c->d_plan);
+    if (c->d_part) cudaFree(c->d_part);
+    if (c->h_plan) cudaFreeHost(c->h_plan);
+    if (c->upload_done) cudaEventDestroy(c->upload_done);
+  }
+  delete c->open;
+  delete c;
+  return PIE_OK;
+}
+
+pie_status pie_ws_create(pie_ctx* c, pie_ws* out) {
+  if (!c || !out) return PIE_ERR_INVALID;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is open");
+  *out = c->next_ws++;
+  c->ws.emplace(*out, WorkingSet{});
+  return PIE_OK;
+}
+
+pie_status pie_ws_destroy(pie_ctx* c, pie_ws h) {
+  if (!c) return PIE_ERR_INVALID;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is open");
+  WorkingSet* w = find_ws(c, h);
+  if (!w) return fail(c, PIE_ERR_BAD_HANDLE, "no working set %d", h);
+  release_from(c, *w, 0);
+  c->ws.erase(h);
+  return PIE_OK;
+}
+
+pie_status pie_ws_fork(pie_ctx* c, pie_ws parent, pie_ws* child) {
+  if (!c || !child) return PIE_ERR_INVALID;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is open");
+  WorkingSet* p = find_ws(c, parent);
+  if (!p) return fail(c, PIE_ERR_BAD_HANDLE, "no working set %d", parent);
+  WorkingSet w;
+  w.n_frozen = p->n_frozen;
+  w.tokens.assign(p->tokens.begin(), p->tokens.begin() + p->n_frozen);
+  w.pages.assign(p->pages.begin(), p->pages.begin() + cdiv(p->n_frozen, kPageSize));
+  for (int32_t pg : w.pages) c->refcount[pg] += 1;
+  *child = c->next_ws++;
+  c->ws.emplace(*child, std::move(w));
+  return PIE_OK;
+}
+
+pie_status pie_ws_freeze(pie_ctx* c, pie_ws h, int32_t n) {
+  if (!c) return PIE_ERR_INVALID;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is open");
+  WorkingSet* w = find_ws(c, h);
+  if (!w) return fail(c, PIE_ERR_BAD_HANDLE, "no working set %d", h);
+  int32_t writable = w->n_tokens() - w->n_frozen;
+  if (n < 0) n = writable;
+  if (n > writable) return fail(c, PIE_ERR_RANGE, "freeze %d > %d writable tokens", n, writable);
+  int32_t old_full = w->n_frozen / kPageSize;
+  w->n_frozen += n;
+  for (int32_t i = old_full; i < w->n_frozen / kPageSize; ++i) {
+    int32_t page = w->pages[i];
+    if (c->page_key.count(page)) continue;
+    DedupKey key;
+    bool known = true;
+    for (int32_t j = 0; j < kPageSize; ++j) {
+      key.v[1 + j] = w->tokens[i * kPageSize + j];
+      known = known && key.v[1 + j] >= 0;
+    }
+    if (!known) continue;
+    key.v[0] = i == 0 ? -1 : w->pages[i - 1];
+    if (i > 0 && !c->page_key.count(key.v[0])) continue;
+    if (c->dedup.count(key)) continue;
+    c->dedup.emplace(key, page);
+    c->page_key.emplace(page, key);
+  }
+  return PIE_OK;
+}
+
+pie_status pie_ws_rollback(pie_ctx* c, pie_ws h, int32_t n) {
+  if (!c) return PIE_ERR_INVALID;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is open");
+  WorkingSet* w = find_ws(c, h);
+  if (!w) return fail(c, PIE_ERR_BAD_HANDLE, "no working set %d", h);
+  if (n < 0 || n > w->n_tokens() - w->n_frozen)
+    return fail(c, PIE_ERR_RANGE, "rollback %d > %d writable tokens", n, w->n_tokens() - w->n_frozen);
+  w->tokens.resize(w->tokens.size() - n);
+  release_from(c, *w, cdiv(w->n_tokens(), kPageSize));
+  return PIE_OK;
+}
+
+pie_status pie_ws_match_prefix(pie_ctx* c, pie_ws h, const int32_t* toks, int32_t n, int32_t* n_reused) {
+  if (!c || n < 0 || (n > 0 && !toks)) return PIE_ERR_INVALID;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is open");
+  WorkingSet* w = find_ws(c, h);
+  if (!w) return fail(c, PIE_ERR_BAD_HANDLE, "no working set %d", h);
+  if (w->n_tokens()) return fail(c, PIE_ERR_STATE, "match_prefix needs an empty working set");
+  int32_t parent = -1, matched = 0;
+  while ((matched + 1) * kPageSize <= n) {
+    DedupKey key;
+    key.v[0] = parent;
+    for (int32_t j = 0; j < kPageSize; ++j) key.v[1 + j] = toks[matched * kPageSize + j];
+    auto it = c->dedup.find(key);
+    if (it == c->dedup.end()) break;
+    w->pages.push_back(it->second);
+    c->refcount[it->second] += 1;
+    parent = it->second;
+    ++matched;
+  }
+  w->tokens.assign(toks, toks + matched * kPageSize);
+  w->n_frozen = matched * kPageSize;
+  if (n_reused) *n_reused = matched * kPageSize;
+  return PIE_OK;
+}
+
+pie_status pie_ws_info(const pie_ctx* c, pie_ws h, int32_t* nt, int32_t* nf, int32_t* np) {
+  if (!c) return PIE_ERR_INVALID;
+  auto it = c->ws.find(h);
+  if (it == c->ws.end()) return PIE_ERR_BAD_HANDLE;
+  if (nt) *nt = it->second.n_tokens();
+  if (nf) *nf = it->second.n_frozen;
+  if (np) *np = static_cast<int32_t>(it->second.pages.size());
+  return PIE_OK;
+}
+
+pie_status pie_ws_page_table(const pie_ctx* c, pie_ws h, int32_t* out, int32_t cap, int32_t* n) {
+  if (!c) return PIE_ERR_INVALID;
+  auto it = c->ws.find(h);
+  if (it == c->ws.end()) return PIE_ERR_BAD_HANDLE;
+  const auto& p = it->second.pages;
+  int32_t m = std::min<int32_t>(cap, static_cast<int32_t>(p.size()));
+  if (out && m > 0) std::memcpy(out, p.data(), m * sizeof(int32_t));
+  if (n) *n = static_cast<int32_t>(p.size());
+  return PIE_OK;
+}
+
+pie_status pie_page_refcount(const pie_ctx* c, int32_t page, int32_t* rc) {
+  if (!c || !rc || page < 0 || page >= c->geo.num_pages) return PIE_ERR_INVALID;
+  *rc = c->refcount[page];
+  return PIE_OK;
+}
+
+pie_status pie_free_pages(const pie_ctx* c, int32_t* n) {
+  if (!c || !n) return PIE_ERR_INVALID;
+  *n = static_cast<int32_t>(c->free_stack.size());
+  return PIE_OK;
+}
+
+pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_batch** out) {
+  if (!c || !out || n_segs < 0 || (n_segs > 0 && !segs)) return PIE_ERR_INVALID;
+  *out = nullptr;
+  if (c->open) return fail(c, PIE_ERR_STATE, "a batch is already open");
+  // validate and count pages, touching nothing
+  std::unordered_set<int32_t> seen;
+  int64_t need = 0, n_rows = 0;
+  for (int32_t i = 0; i < n_segs; ++i) {
+    const pie_seg& s = segs[i];
+    WorkingSet* w = find_ws(c, s.ws);
+    if (!w) return fail(c, PIE_ERR_BAD_HANDLE, "segment %d: no working set %d", i, s.ws);
+    if (!seen.insert(s.ws).second) return fail(c, PIE_ERR_INVALID, "working set %d twice in one pass", s.ws);
+    if (s.n_new < 0) return fail(c, PIE_ERR_INVALID, "segment %d: n_new < 0", i);
+    if (s.n_new == 0) continue;
+    int32_t n0 = w->n_tokens();
+    need += cdiv(static_cast<int64_t>(n0) + s.n_new, kPageSize) - cdiv(n0, kPageSize);
+    if (n0 % kPageSize && c->refcount[w->pages[n0 / kPageSize]] > 1) need += 1;
+    n_rows += s.n_new;
+  }
+  if (need > static_cast<int64_t>(c->free_stack.size()))
+    return fail(c, PIE_ERR_NO_PAGES, "pass needs %lld pages, %zu free", static_cast<long long>(need),
+                c->free_stack.size());
+  if (n_rows > INT32_MAX / 2) return fail(c, PIE_ERR_INVALID, "too many rows");
+
+  // reserve slots
+  auto* b = new pie_batch();
+  b->ctx = c;
+  b->n_rows = static_cast<int32_t>(n_rows);
+  PlanBuilder pb;
+  std::vector<SegInfo> infos;
+  b->row_pos.reserve(n_rows);
+  b->row_slot.reserve(n_rows);
+  for (int32_t i = 0; i < n_segs; ++i) {
+    const pie_seg& s = segs[i];
+    if (s.n_new == 0) continue;
+    WorkingSet& w = c->ws[s.ws];
+    int32_t n0 = w.n_tokens();
+    if (n0 % kPageSize) {
+      int32_t tail = w.pages[n0 / kPageSize];
+      if (c->refcount[tail] > 1) {
+        int32_t fresh = alloc_page(c);
+        c->refcount[tail] -= 1;
+        w.pages[n0 / kPageSize] = fresh;
+        pb.copies.push_back({tail, fresh});
+      }
+    }
+    SegInfo si{};
+    si.seg = i;
+    si.n0 = n0;
+    si.n_new = s.n_new;
+    si.row0 = static_cast<int32_t>(b->row_pos.size());
+    si.group = -1;
+    for (int32_t t = 0; t < s.n_new; ++t) {
+      int32_t pos = n0 + t;
+      if (pos % kPageSize == 0) w.pages.push_back(alloc_page(c));
+      b->row_pos.push_back(pos);
+      b->row_slot.push_back(w.pages[pos / kPageSize] * kPageSize + pos % kPageSize);
+    }
+    for (int32_t t = 0; t < s.n_new; ++t) w.tokens.push_back(s.token_ids ? s.token_ids[t] : -1);
+    si.table_off = static_cast<int32_t>(pb.page_ids.size());
+    si.n_pages = static_cast<int32_t>(w.pages.size());
+    pb.page_ids.insert(pb.page_ids.end(), w.pages.begin(), w.pages.end());
+    infos.push_back(si);
+  }
+  pb.row_list.resize(n_rows);
+  for (int32_t r = 0; r < n_rows; ++r) pb.row_list[r] = r;
+  build_plan(c, infos, b->n_rows, pb);
+  pb.row_pos = b->row_pos;
+  pb.row_slot = b->row_slot;
+  b->dec = pb.dec;
+  b->pre = pb.pre;
+
+  // lay out and upload
+  std::vector<uint8_t> blob;
+  size_t o_pages = put(blob, pb.page_ids), o_pos = put(blob, pb.row_pos), o_slot = put(blob, pb.row_slot);
+  size_t o_base = put(blob, pb.row_part_base), o_list = put(blob, pb.row_list);
+  size_t o_mr = put(blob, pb.merge_rows), o_mn = put(blob, pb.merge_nparts);
+  size_t o_cp = put(blob, pb.copies), o_dec = put(blob, pb.dec, 32), o_pre = put(blob, pb.pre, 32);
+  int64_t total_parts = 0;
+  for (int32_t n : pb.merge_nparts) total_parts += n;
+
+  pie::PlanView& v = b->view;
+  v.n_rows = b->n_rows;
+  v.n_dec = static_cast<int32_t>(pb.dec.size());
+  v.n_pre = static_cast<int32_t>(pb.pre.size());
+  v.n_merge = static_cast<int32_t>(pb.merge_rows.size());
+  v.n_copies = static_cast<int32_t>(pb.copies.size());
+  if (!c->plan_only && !blob.empty()) {
+    pie_status st = ensure_device(c, &c->d_plan, &c->plan_cap, blob.size());
+    size_t part_need = static_cast<size_t>(total_parts) * c->geo.hq * (c->geo.d + 2);
+    if (st == PIE_OK) st = ensure_device(c, &c->d_part, &c->part_cap, std::max<size_t>(part_need, 1));
+    if (st == PIE_OK && c->upload_pending) {
+      cudaError_t e = cudaEventSynchronize(c->upload_done);
+      if (e != cudaSuccess) st = cuda_fail(c, e, "cudaEventSynchronize");
+      c->upload_pending = false;
+    }
+    if (st == PIE_OK && blob.size() > c->h_plan_cap) {
+      if (c->h_plan) cudaFreeHost(c->h_plan);
+      c->h_plan = nullptr;
+      c->h_plan_cap = 0;
+      size_t n = std::max(blob.size(), c->h_plan_cap + c->h_plan_cap / 2);
+      cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&c->h_plan), n);
+      if (e != cudaSuccess) st = cuda_fail(c, e, "cudaMallocHost");
+      else c->h_plan_cap = n;
+    }
+    if (st == PIE_OK) {
+      std::memcpy(c->h_plan, blob.data(), blob.size());
+      cudaError_t e = cudaMemcpyAsync(c->d_plan, c->h_plan, blob.size(), cudaMemcpyHostToDevice, c->stream);
+      if (e == cudaSuccess) e = cudaEventRecord(c->upload_done, c->stream);
+      if (e != cudaSuccess) st = cuda_fail(c, e, "plan upload");
+      c->upload_pending = e == cudaSuccess;
+    }
+    if (st != PIE_OK) {
+      // The host state already moved; a CUDA failure here leaves the
+      // context unusable for device work, which the error reports.
+      c->open = b;
+      return st;
+    }
+    uint8_t* d = c->d_plan;
+    v.page_ids = reinterpret_cast<const int32_t*>(d + o_pages);
+    v.row_pos = reinterpret_cast<const int32_t*>(d + o_pos);
+    v.row_slot = reinterpret_cast<const int32_t*>(d + o_slot);
+    v.row_part_base = reinterpret_cast<const int32_t*>(d + o_base);
+    v.row_list = reinterpret_cast<const int32_t*>(d + o_list);
+    v.merge_rows = reinterpret_cast<const int32_t*>(d + o_mr);
+    v.merge_nparts = reinterpret_cast<const int32_t*>(d + o_mn);
+    v.copies = reinterpret_cast<const CopyItem*>(d + o_cp);
+    v.dec_items = reinterpret_cast<const WorkItem*>(d + o_dec);
+    v.pre_items = reinterpret_cast<const WorkItem*>(d + o_pre);
+    if (v.n_copies) {
+      cudaError_t e = pie::launch_page_copy(c->geo, v, c->cfg.k_pool, c->cfg.v_pool, c->stream);
+      if (e != cudaSuccess) {
+        c->open = b;
+        return cuda_fail(c, e, "page copy launch");
+      }
+    }
+  }
+  c->open = b;
+  *out = b;
+  return PIE_OK;
+}
+
+pie_status pie_batch_rows(const pie_batch* b, int32_t* n) {
+  if (!b || !n) return PIE_ERR_INVALID;
+  *n = b->n_rows;
+  return PIE_OK;
+}
+
+pie_status pie_batch_slots(const pie_batch* b, int32_t* pos, int32_t* slot) {
+  if (!b) return PIE_ERR_INVALID;
+  if (pos && b->n_rows) std::memcpy(pos, b->row_pos.data(), b->n_rows * sizeof(int32_t));
+  if (slot && b->n_rows) std::memcpy(slot, b->row_slot.data(), b->n_rows * sizeof(int32_t));
+  return PIE_OK;
+}
+
+pie_status pie_kv_append(pie_ctx* c, pie_batch* b, int32_t layer, const void* k, const void* v) {
+  if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
+  if (layer < 0 || layer >= c->geo.num_layers) return fail(c, PIE_ERR_INVALID, "layer %d", layer);
+  if (b->n_rows == 0) return PIE_OK;
+  if (!k || !v) return fail(c, PIE_ERR_INVALID, "null K or V");
+  const int32_t nsc = c->geo.num_layers * c->geo.hkv;
+  cudaError_t e = pie::launch_kv_append(c->geo, b->view, layer, k, v, c->cfg.k_pool, c->cfg.v_pool,
+                                        c->d_scales + 2 * nsc, c->d_scales + 3 * nsc, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "kv_append launch");
+  b->appended_any = true;
+  return PIE_OK;
+}
+
+pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, void* out, float* lse) {
+  if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
+  if (layer < 0 || layer >= c->geo.num_layers) return fail(c, PIE_ERR_INVALID, "layer %d", layer);
+  if (b->n_rows == 0) return PIE_OK;
+  if (!q || !out) return fail(c, PIE_ERR_INVALID, "null Q or output");
+  const pie::PlanView& v = b->view;
+  const int32_t nsc = c->geo.num_layers * c->geo.hkv;
+  float* acc = c->d_part;
+  size_t total_parts = c->part_cap / (static_cast<size_t>(c->geo.hq) * (c->geo.d + 2));
+  float* ml = c->d_part + total_parts * c->geo.hq * c->geo.d;
+  cudaError_t e = cudaSuccess;
+  if (v.n_pre)
+    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, out, lse, acc, ml, c->d_err,
+                            c->stream);
+  if (e == cudaSuccess && v.n_dec)
+    e = pie::launch_decode(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
+                           lse, acc, ml, c->d_err, c->stream);
+  if (e == cudaSuccess && v.n_merge) e = pie::launch_merge(c->geo, v, out, lse, acc, ml, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "attend launch");
+  return PIE_OK;
+}
+
+pie_status pie_ctx_check(pie_ctx* c, int32_t* flags) {
+  if (!c || !flags) return PIE_ERR_INVALID;
+  *flags = 0;
+  if (c->plan_only) return PIE_OK;
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e == cudaSuccess) e = cudaMemcpy(flags, c->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(c, e, "pie_ctx_check");
+  return PIE_OK;
+}
+
+pie_status pie_batch_plan_info(const pie_batch* b, int32_t* info) {
+  if (!b || !info) return PIE_ERR_INVALID;
+  info[0] = b->view.n_dec;
+  info[1] = b->view.n_pre;
+  info[2] = b->view.n_merge;
+  info[3] = b->view.n_copies;
+  return PIE_OK;
+}
+
+pie_status pie_batch_items(const pie_batch* b, int32_t kind, int32_t* out, int32_t cap, int32_t* n) {
+  if (!b || !n || (kind != 0 && kind != 1)) return PIE_ERR_INVALID;
+  const auto& v = kind == 0 ? b->dec : b->pre;
+  *n = static_cast<int32_t>(v.size());
+  int32_t m = std::min<int32_t>(cap, *n);
+  if (out && m > 0) std::memcpy(out, v.data(), static_cast<size_t>(m) * sizeof(WorkItem));
+  return PIE_OK;
+}
+
+pie_status pie_batch_end(pie_ctx* c, pie_batch* b) {
+  if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  delete b;
+  c->open = nullptr;
+  return PIE_OK;
+}
+
+}  // extern "C"

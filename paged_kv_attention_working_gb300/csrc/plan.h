@@ -1,0 +1,69 @@
+// Internal plan structures shared by the host planner and the CUDA kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pie {
+
+constexpr int kPageSize = 16;
+
+// One unit of attention work for one KV head (the head is blockIdx.y): a set
+// of query rows that all read the same run of pages of one working set.
+// Private items cover one segment's rows over part of its own pages; shared
+// items cover the rows of every segment of a fork/dedup group over the
+// pages they all hold.
+struct WorkItem {
+  int32_t pages_off;  // index into page_ids of the first page of the run
+  int32_t n_pages;    // pages in the run
+  int32_t key_base;   // position of the run's first key (16 * logical page)
+  int32_t rows_off;   // index into row_list of the item's first row
+  int32_t n_rows;     // rows (each row contributes Hq/Hkv query heads)
+  int32_t part;       // -1: rows are written straight to the output;
+                      // else partial index = row_part_base[row] + part
+  int32_t n_keys;     // keys in the run that lie before its end (<= 16*n_pages)
+  int32_t pad;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+struct CopyItem {  // copy-on-write: page src -> page dst, every layer, K and V
+  int32_t src, dst;
+};
+
+// Device views of one batch's plan (all arrays live in one uploaded buffer).
+struct PlanView {
+  const int32_t* page_ids;
+  const int32_t* row_pos;        // [n_rows]
+  const int32_t* row_slot;       // [n_rows] page * 16 + slot
+  const int32_t* row_part_base;  // [n_rows], -1 for direct rows
+  const int32_t* row_list;       // item row lists
+  const WorkItem* dec_items;     // decode-kernel items
+  const WorkItem* pre_items;     // tensor-core (prefill) items
+  const int32_t* merge_rows;     // rows with >= 2 parts
+  const int32_t* merge_nparts;
+  const CopyItem* copies;
+  int32_t n_rows, n_dec, n_pre, n_merge, n_copies;
+};
+
+struct Geometry {
+  int32_t num_layers, hq, hkv, d, num_pages, kv_dtype;
+  int64_t block_bytes;  // 16 * d * esize
+};
+
+// Kernel launchers (defined in the .cu files); all return cudaGetLastError().
+cudaError_t launch_kv_append(const Geometry& g, const PlanView& p, int layer,
+                             const void* k, const void* v, void* kpool, void* vpool,
+                             const float* inv_scale_k, const float* inv_scale_v,
+                             cudaStream_t st);
+cudaError_t launch_page_copy(const Geometry& g, const PlanView& p, void* kpool, void* vpool,
+                             cudaStream_t st);
+cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const void* q,
+                          const void* kpool, const void* vpool, const float* scale_k,
+                          const float* scale_v, void* out, float* lse, float* part_acc,
+                          float* part_ml, int* err, cudaStream_t st);
+cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, const void* q,
+                           const void* kpool, const void* vpool, void* out, float* lse,
+                           float* part_acc, float* part_ml, int* err, cudaStream_t st);
+cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float* lse,
+                         const float* part_acc, const float* part_ml, cudaStream_t st);
+
+}  // namespace pie

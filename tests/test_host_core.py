@@ -1,0 +1,264 @@
+"""The C++ host core (through the C ABI, plan-only contexts, no GPU) against
+the oracle's working-set model: bit-exact page tables, reference counts,
+slot maps and error statuses; plus the planner's work decomposition."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle_driver
+from oracle import kvstore
+from oracle.kvstore import OracleError
+from paged_kv_attention_working_gb300 import pie
+from paged_kv_attention_working_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_library_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "pie_attn.h")).read()
+    declared = set(re.findall(r"^\s*(?:pie_status|const char\*)\s+(pie_\w+)\s*\(", header, re.M))
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(pie.lib, name), name
+    assert declared <= set(pie.EXPORTS) | {"pie_last_error"}
+
+
+class Twin:
+    """Same operations on the oracle model and on a plan-only library context."""
+
+    def __init__(self, P, free_list, hq=4, hkv=2, d=64):
+        self.o = kvstore.KVStore(1, hq, hkv, d, P, free_list=free_list, with_pool=False)
+        self.c = pie.pie_ctx_create(1, hq, hkv, d, P, free_list=free_list, num_sms=152)
+
+    def call(self, name, *args):
+        err_o = err_c = None
+        try:
+            ro = getattr(self.o, name)(*args)
+        except OracleError as e:
+            err_o, ro = e.status, None
+        cargs = [self.c] + list(args)
+        try:
+            if name == "begin":
+                b = pie.pie_batch_begin(self.c, args[0])
+                rc = pie.pie_batch_slots(b)
+                pie.pie_batch_end(self.c, b)
+            else:
+                rc = getattr(pie, "pie_" + name)(*cargs)
+        except pie.PieError as e:
+            err_c, rc = e.status, None
+        assert err_o == err_c, (name, args, err_o, err_c)
+        if name == "begin" and ro is not None:
+            assert (ro.rows_pos, ro.rows_slot) == tuple(rc)
+        elif name in ("ws_create", "ws_fork", "ws_match_prefix") and ro is not None:
+            assert ro == rc
+        return ro
+
+    def compare(self):
+        assert pie.pie_free_pages(self.c) == len(self.o.free)
+        for p in range(self.o.P):
+            assert pie.pie_page_refcount(self.c, p) == self.o.refcount[p], p
+        for h in self.o.ws:
+            assert pie.pie_ws_page_table(self.c, h) == self.o.ws_page_table(h)
+            assert pie.pie_ws_info(self.c, h) == self.o.ws_info(h)
+
+    def close(self):
+        pie.pie_ctx_destroy(self.c)
+
+
+def test_random_operation_sequences_bit_exact():
+    rng = np.random.default_rng(2024)
+    for trial in range(25):
+        P = int(rng.integers(4, 48))
+        t = Twin(P, rng.permutation(P).tolist())
+        live = []
+        for step in range(80):
+            op = int(rng.integers(0, 8))
+            if op == 0 or not live:
+                live.append(t.call("ws_create"))
+            elif op == 1:
+                h = t.call("ws_fork", live[rng.integers(len(live))])
+                if h is not None:
+                    live.append(h)
+            elif op in (2, 7):
+                segs = []
+                for h in rng.permutation(live)[: rng.integers(1, len(live) + 1)]:
+                    n = int(rng.integers(0, 40))
+                    toks = rng.integers(0, 2, n).tolist() if rng.random() < 0.7 else None
+                    segs.append((int(h), n, toks))
+                if rng.random() < 0.05 and segs:
+                    segs.append(segs[0])          # duplicate working set: rejected
+                t.call("begin", segs)
+            elif op == 3:
+                t.call("ws_freeze", live[rng.integers(len(live))], int(rng.integers(-1, 30)))
+            elif op == 4:
+                t.call("ws_rollback", live[rng.integers(len(live))], int(rng.integers(0, 20)))
+            elif op == 5:
+                h = live.pop(rng.integers(len(live)))
+                t.call("ws_destroy", h)
+            elif op == 6:
+                h = t.call("ws_create")
+                live.append(h)
+                t.call("ws_match_prefix", h, rng.integers(0, 2, int(rng.integers(0, 70))).tolist())
+            t.compare()
+        t.call("ws_destroy", 10 ** 6)            # bad handle on both sides
+        t.close()
+
+
+@pytest.mark.parametrize("name", list(wl.FULL))
+def test_workload_scripts_bit_exact(name):
+    w = wl.reduced(name)
+    c = pie.pie_ctx_create(w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages,
+                           kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
+                           k_scale=w.scales()[0], v_scale=w.scales()[1])
+    handles = {}
+    store = oracle_driver.make_store(w, with_pool=False)
+    ohandles = {}
+    for op in w.ops:
+        k = op[0]
+        if k == "create":
+            handles[op[1]] = pie.pie_ws_create(c)
+            ohandles[op[1]] = store.ws_create()
+        elif k == "fork":
+            handles[op[2]] = pie.pie_ws_fork(c, handles[op[1]])
+            ohandles[op[2]] = store.ws_fork(ohandles[op[1]])
+        elif k == "freeze":
+            pie.pie_ws_freeze(c, handles[op[1]], op[2])
+            store.ws_freeze(ohandles[op[1]], op[2])
+        elif k == "rollback":
+            pie.pie_ws_rollback(c, handles[op[1]], op[2])
+            store.ws_rollback(ohandles[op[1]], op[2])
+        elif k == "match":
+            toks = w.tok_stream(op[2]).tolist()
+            assert pie.pie_ws_match_prefix(c, handles[op[1]], toks) == store.ws_match_prefix(ohandles[op[1]], toks)
+        elif k == "pass":
+            pas = store.begin([(ohandles[s[0]], s[1], w.gather_tok(s[4])) for s in op[1]])
+            b = pie.pie_batch_begin(c, [(handles[s[0]], s[1], w.gather_tok(s[4])) for s in op[1]])
+            assert pie.pie_batch_slots(b) == (pas.rows_pos, pas.rows_slot)
+            assert pie.pie_batch_plan_info(b)["copies"] == len(pas.cow)
+            pie.pie_batch_end(c, b)
+    for name_, h in handles.items():
+        assert pie.pie_ws_page_table(c, h) == store.ws_page_table(ohandles[name_])
+    for p in range(w.num_pages):
+        assert pie.pie_page_refcount(c, p) == store.refcount[p]
+    pie.pie_ctx_destroy(c)
+
+
+def _run_plan(w, upto_pass):
+    """Executes a workload on a plan-only context up to its upto_pass-th pass
+    and returns (ctx, handles, batch) with that pass's batch open."""
+    c = pie.pie_ctx_create(w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages,
+                           kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
+                           k_scale=w.scales()[0], v_scale=w.scales()[1], num_sms=152)
+    hs = {}
+    n = 0
+    for op in w.ops:
+        k = op[0]
+        if k == "create":
+            hs[op[1]] = pie.pie_ws_create(c)
+        elif k == "fork":
+            hs[op[2]] = pie.pie_ws_fork(c, hs[op[1]])
+        elif k == "freeze":
+            pie.pie_ws_freeze(c, hs[op[1]], op[2])
+        elif k == "rollback":
+            pie.pie_ws_rollback(c, hs[op[1]], op[2])
+        elif k == "match":
+            pie.pie_ws_match_prefix(c, hs[op[1]], w.tok_stream(op[2]).tolist())
+        elif k == "pass":
+            b = pie.pie_batch_begin(c, [(hs[s[0]], s[1], w.gather_tok(s[4])) for s in op[1]])
+            if n == upto_pass:
+                return c, hs, b
+            pie.pie_batch_end(c, b)
+            n += 1
+    raise AssertionError("pass not found")
+
+
+def _coverage(c, b, w, hs, segs):
+    """Per row: list of (kind, item) covering it; checks each row's keys
+    0..pos are covered exactly once."""
+    import itertools
+    pos, _ = pie.pie_batch_slots(b)
+    rows_ws = list(itertools.chain.from_iterable([s[0]] * s[1] for s in segs))
+    # reconstruct row lists: identity for private items, group lists after
+    items = [(0, it) for it in pie.pie_batch_items(b, 0)] + [(1, it) for it in pie.pie_batch_items(b, 1)]
+    return pos, rows_ws, items
+
+
+def test_plan_fork_group_reads_shared_pages_once():
+    w = wl.fork_spec(name="fork_plan", seed=3, prompt=4096, n_forks=10, suffix_hi=256, unshared=False)
+    c, hs, b = _run_plan(w, 2)          # the drafts pass: 10 forks x 4 drafts
+    info = pie.pie_batch_plan_info(b)
+    pre = pie.pie_batch_items(b, 1)
+    dec = pie.pie_batch_items(b, 0)
+    # 40 rows x 4 query heads per KV head = 160 > 64: shared prefix on the tensor-core kernel,
+    # one row tile (<= 256), KV split across items; every shared page in exactly one item
+    shared = [it for it in pre if it["key_base"] < 4096 and it["n_rows"] == 40]
+    assert shared and sum(it["n_pages"] for it in shared) == 4096 // 16
+    starts = sorted(it["key_base"] for it in shared)
+    assert starts[0] == 0
+    # private parts: one decode item (4 drafts x 4 heads = 16) per fork
+    assert len([it for it in dec if it["n_rows"] == 4]) >= 10
+    assert info["merge_rows"] == 40
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
+def test_plan_dedup_groups_on_decode_kernel():
+    w = wl.llama70b_fp8(n_ws=16, ctx_lo=2048, ctx_hi=4096, prefix_groups=2)
+    c, hs, b = _run_plan(w, 2)
+    dec = pie.pie_batch_items(b, 0)
+    shared = [it for it in dec if it["n_rows"] == 8]
+    # 8 rows x 8 heads = 64 = four M tiles in one CTA: each shared page once per group
+    assert sum(it["n_pages"] for it in shared) == 2 * (2048 // 16)
+    assert pie.pie_batch_plan_info(b)["prefill_items"] == 0
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
+def test_plan_splits_cover_every_key_once():
+    w = wl.decode_batch(name="split_plan", seed=7, n_ws=64, num_layers=1)
+    c, hs, b = _run_plan(w, 1)
+    dec = pie.pie_batch_items(b, 0)
+    pos, _ = pie.pie_batch_slots(b)
+    per_row = {}
+    for it in dec:
+        assert it["n_rows"] == 1
+        per_row.setdefault(it["rows_off"], []).append((it["key_base"], it["n_pages"], it["part"]))
+    for r, lst in per_row.items():
+        lst.sort()
+        assert lst[0][0] == 0
+        for (a, n, _), (b2, _, _) in zip(lst, lst[1:]):
+            assert a + 16 * n == b2
+        last = lst[-1]
+        assert last[0] + 16 * last[1] >= pos[r] + 1 > last[0] + 16 * (last[1] - 1)
+        parts = sorted(p for _, _, p in lst)
+        assert parts == ([-1] if len(lst) == 1 else list(range(len(lst))))
+    assert len(dec) > 64
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
+def test_plan_only_context_rejects_device_calls():
+    c = pie.pie_ctx_create(1, 4, 2, 64, 8)
+    h = pie.pie_ws_create(c)
+    b = pie.pie_batch_begin(c, [(h, 3, None)])
+    with pytest.raises(pie.PieError) as e:
+        pie.pie_kv_append(c, b, 0, 0, 0)
+    assert e.value.status == pie.PIE_ERR_STATE
+    with pytest.raises(pie.PieError) as e:
+        pie.pie_ws_create(c)                 # batch open
+    assert e.value.status == pie.PIE_ERR_STATE
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
+def test_invalid_configurations_rejected():
+    with pytest.raises(pie.PieError):
+        pie.pie_ctx_create(1, 6, 4, 64, 8)           # Hq not a multiple of Hkv
+    with pytest.raises(pie.PieError):
+        pie.pie_ctx_create(1, 4, 2, 96, 8)           # unsupported head_dim
+    with pytest.raises(pie.PieError):
+        pie.pie_ctx_create(1, 4, 2, 128, 8, kv_dtype=pie.PIE_KV_E4M3)   # e4m3 without scales
+    with pytest.raises(pie.PieError):
+        pie.pie_ctx_create(1, 4, 2, 64, 4, free_list=[0, 1, 1, 2])      # not a permutation
