@@ -48,7 +48,7 @@ def peaks():
 class Clocks:
     """Samples nvidia-smi every 200 ms while the timed region runs."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
@@ -65,24 +65,39 @@ class Clocks:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def mark(self):
+        return time.time()
+
+    def stop(self, t_begin, t_end):
+        """Summary of the samples taken between wall-clock t_begin and t_end."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
         self.proc.terminate()
         self.proc.wait()
         self.f.seek(0)
-        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        rows = [[x.strip() for x in r.split(",")] for r in self.f.read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
-        sm = [float(r[1]) for r in rows if len(r) > 8 and r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if len(r) > 8 and r[2].strip().replace(".", "").isdigit()]
+        import datetime
+
+        def ts(r):
+            try:
+                return datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+
+        inside = [r for r in rows if len(r) > 9 and ts(r) is not None and t_begin - 0.25 <= ts(r) <= t_end + 0.25]
+        num = lambda x: x.replace(".", "").isdigit()
+        sm = [float(r[2]) for r in inside if num(r[2])]
+        mx = [float(r[3]) for r in inside if num(r[3])]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in inside:
             for i, n in enumerate(names):
-                if len(r) > 5 + i and r[5 + i].strip() == "Active":
+                if r[6 + i] == "Active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(inside)}
 
 
 def dist_init():
@@ -115,55 +130,79 @@ def allmax(world, x):
 
 
 # ------------------------------------------------------------ CPU oracle leg
-def oracle_sample(w, seconds=12.0):
-    """Times the oracle's attention on a bounded sample of the workload: the
-    decode rows of the first working sets of one layer, as many as fit in
-    about `seconds`.  Returns (KV GB/s, rows/s, description, cores)."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from oracle import attention, kvstore
+class OracleSample:
+    """The oracle's attention on a bounded sample of the workload: the decode
+    rows of the first working sets of one layer (their real context lengths),
+    each in an oracle store built once; only attend_pass is timed."""
 
-    ctx = w.ctx
-    esize = 2 if w.kv_dtype == 0 else 1
-    rng = np.random.default_rng(0)
-    kv_bytes = rows = 0
-    elapsed = 0.0
-    used = []
-    for i, c in enumerate(ctx):
-        n = c + 1
-        st = kvstore.KVStore(1, w.num_q_heads, w.num_kv_heads, w.head_dim, -(-n // 16) + 1)
-        h = st.ws_create()
+    def __init__(self, w, max_rows=64):
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from oracle import kvstore
         from paged_kv_attention_working_gb300.workloads import bf16_round
 
-        k = bf16_round(rng.standard_normal((n, w.num_kv_heads, w.head_dim), dtype=np.float32))
-        v = bf16_round(rng.standard_normal((n, w.num_kv_heads, w.head_dim), dtype=np.float32))
-        q = bf16_round(rng.standard_normal((1, w.num_q_heads, w.head_dim), dtype=np.float32))
-        p = st.begin([(h, n, None)])
-        st.kv_append(p, 0, k, v)
-        row_pass = kvstore.Pass([h], [n - 1], [p.rows_slot[-1]], [])
-        t0 = time.perf_counter()
-        attention.attend_pass(st, row_pass, 0, kvstore.bf16_bits_to_f64(q))
-        elapsed += time.perf_counter() - t0
-        kv_bytes += n * w.num_kv_heads * w.head_dim * esize * 2
-        rows += 1
-        used.append(c)
-        if elapsed > seconds:
-            break
-    cores = len(os.sched_getaffinity(0))
-    desc = (f"oracle attend_pass (float64 numpy, page gather + exact softmax) on {rows} decode rows "
-            f"(contexts {used[:4]}{'...' if len(used) > 4 else ''}) of one layer of the workload")
-    return kv_bytes / elapsed / 1e9, rows / elapsed, desc, cores, elapsed
+        self.w = w
+        self.kvstore = kvstore
+        rng = np.random.default_rng(0)
+        self.items = []
+        self.max_rows = max_rows
+        self.rng, self.bf16_round = rng, bf16_round
+
+    def _item(self, i):
+        w, kvstore = self.w, self.kvstore
+        while len(self.items) <= i:
+            c = w.ctx[len(self.items)]
+            n = c + 1
+            st = kvstore.KVStore(1, w.num_q_heads, w.num_kv_heads, w.head_dim, -(-n // 16) + 1)
+            h = st.ws_create()
+            shape = (n, w.num_kv_heads, w.head_dim)
+            k = self.bf16_round(self.rng.standard_normal(shape, dtype=np.float32))
+            v = self.bf16_round(self.rng.standard_normal(shape, dtype=np.float32))
+            q = self.bf16_round(self.rng.standard_normal((1, w.num_q_heads, w.head_dim), dtype=np.float32))
+            p = st.begin([(h, n, None)])
+            st.kv_append(p, 0, k, v)
+            self.items.append((st, kvstore.Pass([h], [n - 1], [p.rows_slot[-1]], []),
+                               kvstore.bf16_bits_to_f64(q), c))
+        return self.items[i]
+
+    def run(self, seconds):
+        """Returns (KV GB/s, rows/s, description, cores, elapsed)."""
+        from oracle import attention
+
+        esize = 2 if self.w.kv_dtype == 0 else 1
+        kv_bytes = rows = 0
+        elapsed = 0.0
+        used = []
+        for i in range(min(self.max_rows, len(self.w.ctx))):
+            st, pas, q, c = self._item(i)
+            t0 = time.perf_counter()
+            attention.attend_pass(st, pas, 0, q)
+            elapsed += time.perf_counter() - t0
+            kv_bytes += (c + 1) * self.w.num_kv_heads * self.w.head_dim * esize * 2
+            rows += 1
+            used.append(c)
+            if elapsed > seconds:
+                break
+        cores = len(os.sched_getaffinity(0))
+        desc = (f"oracle attend_pass (float64 numpy, page gather + exact softmax) on {rows} decode rows "
+                f"(contexts {used[:4]}{'...' if len(used) > 4 else ''}) of one layer of the workload; "
+                f"numpy default BLAS threading")
+        return kv_bytes / elapsed / 1e9, rows / elapsed, desc, cores, elapsed
 
 
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
-    per_step = []
-    gbs = rps = None
+    per_step, gbs_l, rps_l = [], [], []
     desc = cores = None
+    sample = OracleSample(w)
+    step_s = max(0.2, args.ref_seconds / max(1, args.warmup + args.steps))
     for i in range(args.warmup + args.steps):
-        gbs, rps, desc, cores, el = oracle_sample(w, seconds=args.ref_seconds)
+        gbs, rps, desc, cores, el = sample.run(step_s)
         if i >= args.warmup:
             per_step.append(el)
+            gbs_l.append(gbs)
+            rps_l.append(rps)
+    gbs, rps = statistics.median(gbs_l), statistics.median(rps_l)
     line = {"impl": "reference", "metric": "decode attend KV GB/s", "value": gbs, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(per_step), "higher_is_better": True, "scaling": "weak",
@@ -189,8 +228,8 @@ def run_gpu(args, w, world, rank, local):
     esize = 2 if w.kv_dtype == 0 else 1
     block = 16 * D * esize
     pool_bytes = L * w.num_pages * Hkv * block
-    kpool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
-    vpool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
+    kpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+    vpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
     ks, vs = w.scales()
     ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
                              k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
@@ -248,17 +287,19 @@ def run_gpu(args, w, world, rank, local):
         for n in names:
             pie.pie_ws_rollback(ctx, hs[n], 1)
 
+    clocks = Clocks(local)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     assert pie.pie_ctx_check(ctx) == 0
+    time.sleep(0.5)  # let the clock sampler start before the timed region
 
     # ---- device-resident timing
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)] for _ in range(args.steps)]
-    clocks = Clocks(local)
     barrier(world)
     torch.cuda.synchronize(dev)
-    clocks.start()
+    wall0 = time.time()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -266,7 +307,8 @@ def run_gpu(args, w, world, rank, local):
         step(events[s])
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
     barrier(world)
     ms = t0.elapsed_time(t1) / args.steps
     ms = allmax(world, ms)
@@ -322,15 +364,18 @@ def run_gpu(args, w, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=20.0,
+                    help="CPU seconds of oracle work (whole reference run, or the cpu_baseline sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
     args = ap.parse_args()
     from paged_kv_attention_working_gb300 import workloads as wl
 
-    w = wl.llama8b_decode()
+    w = wl.llama8b_decode(num_layers=args.layers)
     world, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, w, world, rank)
@@ -338,7 +383,7 @@ def main():
     result = run_gpu(args, w, world, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            gbs, rps, desc, cores, _ = oracle_sample(w, seconds=args.ref_seconds)
+            gbs, rps, desc, cores, _ = OracleSample(w).run(args.ref_seconds)
             result["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                       "sample": desc, "rows_per_s": rps}
         print(json.dumps(result), flush=True)

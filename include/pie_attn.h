@@ -38,6 +38,11 @@
  *  little-endian bit patterns; e4m3 elements (OCP FP8 E4M3) are
  *  round-to-nearest-even, saturating encodings of float32(x) * float32(1 /
  *  scale[layer][kv_head]).
+ *  The pools must be initialised (zeroed, say) before first use: the
+ *  kernels read whole pages, and slots past a working set's length enter
+ *  the tensor-core products with zero weight, so a non-finite value there
+ *  would turn the result into NaN.  Slots the library writes always hold
+ *  the appended (finite) values or copies of them.
  */
 #ifndef PIE_ATTN_H
 #define PIE_ATTN_H
