@@ -361,6 +361,101 @@ def run_gpu(args, w, world, rank, local):
     return result
 
 
+def run_mixed(args, w, world, rank, local):
+    """Mixed continuous batch (16 prefill chunks + 128 decode rows, one
+    pie_attend): times the whole step, and the chunks alone (the tensor-core
+    prefill kernel alone, every row written directly) for its TFLOP/s."""
+    import torch
+
+    from paged_kv_attention_working_gb300 import pie
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+    block = 16 * D * 2
+    pool_bytes = w.num_layers * w.num_pages * Hkv * block
+    kpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+    vpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+    ctx = pie.pie_ctx_create(w.num_layers, Hq, Hkv, D, w.num_pages, free_list=w.free_list().tolist(),
+                             k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000 + rank)
+    hs = {}
+    for op in w.ops:
+        if op[0] == "create":
+            hs[op[1]] = pie.pie_ws_create(ctx)
+    fill = [op for op in w.ops if op[0] == "pass"][0][1]
+    main_segs = [op for op in w.ops if op[0] == "pass"][1][1]
+    b = pie.pie_batch_begin(ctx, [(hs[s[0]], s[1], None) for s in fill])
+    n = pie.pie_batch_rows(b)
+    k = torch.randn((n, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    pie.pie_kv_append(ctx, b, 0, k, k)
+    pie.pie_batch_end(ctx, b)
+    del k
+    for name in hs:
+        pie.pie_ws_freeze(ctx, hs[name], -1)
+
+    def make(segs):
+        rows = sum(s[1] for s in segs)
+        q = torch.randn((rows, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
+        kv = torch.randn((rows, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty((rows, Hq, D), dtype=torch.bfloat16, device=dev)
+        return q, kv, out
+
+    chunk_segs = [s for s in main_segs if s[0].startswith("c")]
+    flops = 0
+    for s, c0 in zip(chunk_segs, w.chunk_ctx):
+        nn = s[1]
+        flops += 4 * D * Hq * (nn * c0 + nn * (nn + 1) // 2)
+    dec_keys = sum(c + 1 for c in w.decode_ctx)
+
+    def timed(segs, tensors, steps):
+        q, kv, out = tensors
+        evs = []
+        for i in range(args.warmup + steps):
+            bb = pie.pie_batch_begin(ctx, [(hs[s[0]], s[1], None) for s in segs])
+            pie.pie_kv_append(ctx, bb, 0, kv, kv)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pie.pie_attend(ctx, bb, 0, q, out)
+            e1.record(stream)
+            pie.pie_batch_end(ctx, bb)
+            for s in segs:
+                pie.pie_ws_rollback(ctx, hs[s[0]], s[1])
+            if i >= args.warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        assert pie.pie_ctx_check(ctx) == 0
+        return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
+
+    t_chunks = timed(chunk_segs, make(chunk_segs), args.steps)
+    t_mixed = timed(main_segs, make(main_segs), args.steps)
+    tflops = flops / (t_chunks * 1e-3) / 1e12
+    peak = FALLBACK_BF16_TFLOPS
+    src = "fallback"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("bf16_tflops"):
+            peak, src = float(d["bf16_tflops"]), "measured"
+    res = {"metric": "prefill attend TFLOP/s (causal-exact flops)", "value": tflops, "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mixed,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic",
+           "config": {"workload": w.name, "chunks": len(chunk_segs), "chunk_rows": sum(s[1] for s in chunk_segs),
+                      "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1},
+           "roofline": {"bound": "tensor", "kernel": "prefill_kernel (chunks-only attend)", "achieved": tflops,
+                        "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": tflops / peak,
+                        "traffic": None, "flops_per_launch": flops, "avg_launch_ms": t_chunks},
+           "mixed_step": {"attend_ms": t_mixed, "rows": sum(s[1] for s in main_segs),
+                          "rows_per_s": sum(s[1] for s in main_segs) / (t_mixed * 1e-3),
+                          "decode_kv_bytes": dec_keys * Hkv * D * 2 * 2}}
+    pie.pie_ctx_destroy(ctx)
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -370,13 +465,19 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=20.0,
                     help="CPU seconds of oracle work (whole reference run, or the cpu_baseline sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="llama8b_decode", choices=["llama8b_decode", "mixed_batch"])
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
     args = ap.parse_args()
     from paged_kv_attention_working_gb300 import workloads as wl
 
-    w = wl.llama8b_decode(num_layers=args.layers)
     world, rank, local = dist_init()
+    if args.workload == "mixed_batch":
+        res = run_mixed(args, wl.mixed_batch(), world, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+    w = wl.llama8b_decode(num_layers=args.layers)
     if args.impl == "reference":
         run_reference(args, w, world, rank)
         return
