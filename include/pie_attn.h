@@ -175,6 +175,59 @@ pie_status pie_attend(pie_ctx* ctx, pie_batch* b, int32_t layer,
 /* Closes the batch.  Its device work stays enqueued on the stream. */
 pie_status pie_batch_end(pie_ctx* ctx, pie_batch* b);
 
+/* ---- decode attention that allocates nothing ----
+ * The paper has no counterpart to this entry point; it is a convenience of
+ * this library.  It serves callers that cannot call cudaMalloc: an engine
+ * that reserved the GPU's memory for its own pool and allocator at start-up
+ * (a library allocation would fail or fragment it), a serving loop that
+ * cannot afford the device-wide synchronisation that cudaMalloc / cudaFree
+ * may imply, or a plug-in whose host runtime forbids foreign allocations.
+ * Such callers need no context (pie_ctx_create allocates): they pass the
+ * pools, a per-row block table and the row lengths themselves.
+ *
+ * Decode attention for rows of one query token each, over bf16 pools in
+ * the layout above: row r attends keys 0..seq_lens[r]-1 of its pages
+ * block_table[r][0..], with the same softmax, head grouping and outputs as
+ * pie_attend.  KV splits and their partial results live in one file-scope
+ * device array of PIE_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
+ * library holds until the process exits.
+ *  - Scratch needed, with S = the KV splits the call picks (S >= 1):
+ *      R*32 + 5*R*4 + (S > 1 ? R*S*(32 + Hq*(head_dim+2)*4) : 0) bytes plus
+ *    alignment; the call lowers S to fit and returns PIE_ERR_RANGE, with
+ *    nothing launched, when even S = 1 does not fit.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the array and leaves its contents behind;
+ *    nothing in it needs to start at zero, because each call writes every
+ *    word it reads before reading it.  Calls that overlap on the GPU (other
+ *    streams, other host threads) race on the array: order them.
+ *  - No cudaMalloc, cudaFree or other allocating call is made.
+ *  - Bounded waits inside the kernel end silently here (there is no context
+ *    to carry an error word).
+ *  - The caller guarantees 1 <= seq_lens[r] <= 16*max_pages_per_row and page
+ *    ids < num_pages; they live on the device and are not checked. */
+#define PIE_NOALLOC_SCRATCH_BYTES (16u << 20)
+typedef struct pie_decode_args {
+  int32_t num_rows;          /* rows (>= 0) */
+  int32_t num_q_heads;       /* Hq */
+  int32_t num_kv_heads;      /* Hkv; Hq/Hkv a power of two <= 64 */
+  int32_t head_dim;          /* 64 or 128 */
+  int32_t num_layers;        /* pool geometry */
+  int32_t num_pages;
+  int32_t layer;
+  int32_t max_pages_per_row; /* row stride of block_table */
+  const void* q;             /* device bf16 [num_rows][Hq][head_dim] */
+  const void* k_pool;        /* device bf16 pools, layout above */
+  const void* v_pool;
+  const int32_t* block_table; /* device [num_rows][max_pages_per_row] */
+  const int32_t* seq_lens;    /* device [num_rows] */
+  void* out;                 /* device bf16 [num_rows][Hq][head_dim] */
+  float* lse;                /* device [num_rows][Hq] or NULL */
+  void* stream;              /* cudaStream_t, NULL = legacy default */
+} pie_decode_args;
+pie_status pie_attend_decode_noalloc(const pie_decode_args* args);
+
 /* ---- introspection (tests, tools) ---- */
 /* info[0..3] = decode-kernel items, tensor-core items, rows merged from
  * several partial results, copy-on-write page copies. */

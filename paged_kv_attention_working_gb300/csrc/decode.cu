@@ -22,7 +22,9 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <mutex>
 
+#include "../../include/pie_attn.h"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -434,3 +436,161 @@ cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float*
 }
 
 }  // namespace pie
+
+// ===========================================================================
+// Decode attention that allocates nothing (pie_attend_decode_noalloc): the
+// same decode and merge kernels, with the KV-split work list and the split
+// partials in a file-scope device array instead of context buffers.
+namespace pie {
+namespace {
+
+constexpr size_t kNoAllocBytes = PIE_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch per device ordinal, looked up once.
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 256;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// One thread per (row, split): the split's work item; split 0 also writes
+// the row's entries.
+__global__ void noalloc_plan(int n_rows, int n_splits, int chunk, int max_pages, const int32_t* __restrict__ seq_lens,
+                             WorkItem* items, int32_t* row_pos, int32_t* row_list, int32_t* part_base,
+                             int32_t* merge_rows, int32_t* merge_np) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_rows * n_splits) return;
+  int r = i / n_splits, s = i % n_splits;
+  int len = seq_lens[r];
+  int pages = (len + kPageSize - 1) / kPageSize;
+  int first = s * chunk;
+  int np = min(chunk, max(0, pages - first));
+  WorkItem it;
+  it.pages_off = r * max_pages + first;
+  it.n_pages = np;
+  it.key_base = first * kPageSize;
+  it.rows_off = r;
+  it.n_rows = 1;
+  it.part = n_splits > 1 ? s : -1;
+  it.n_keys = max(0, min(np * kPageSize, len - first * kPageSize));
+  it.pad = 0;
+  items[i] = it;
+  if (s == 0) {
+    row_pos[r] = len - 1;
+    row_list[r] = r;
+    part_base[r] = n_splits > 1 ? r * n_splits : -1;
+    merge_rows[r] = r;
+    merge_np[r] = n_splits;
+  }
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct NoAllocLayout {
+  size_t items, row_pos, row_list, part_base, merge_rows, merge_np, acc, ml, total;
+};
+
+NoAllocLayout noalloc_layout(int64_t R, int64_t S, int64_t hq, int64_t d) {
+  NoAllocLayout l{};
+  size_t o = 0;
+  l.items = o;
+  o = align256(o + R * S * sizeof(WorkItem));
+  l.row_pos = o;
+  o = align256(o + R * 4);
+  l.row_list = o;
+  o = align256(o + R * 4);
+  l.part_base = o;
+  o = align256(o + R * 4);
+  l.merge_rows = o;
+  o = align256(o + R * 4);
+  l.merge_np = o;
+  o = align256(o + R * 4);
+  l.acc = o;
+  if (S > 1) o = align256(o + R * S * hq * d * 4);
+  l.ml = o;
+  if (S > 1) o = align256(o + R * S * hq * 2 * 4);
+  l.total = o;
+  return l;
+}
+
+}  // namespace
+}  // namespace pie
+
+extern "C" pie_status pie_attend_decode_noalloc(const pie_decode_args* a) {
+  using namespace pie;
+  if (!a) return PIE_ERR_INVALID;
+  const int R = a->num_rows, hq = a->num_q_heads, hkv = a->num_kv_heads, d = a->head_dim;
+  if (R < 0 || hq <= 0 || hkv <= 0 || hq % hkv || (d != 64 && d != 128) || a->num_layers <= 0 ||
+      a->num_pages <= 0 || a->layer < 0 || a->layer >= a->num_layers || a->max_pages_per_row <= 0)
+    return PIE_ERR_INVALID;
+  const int G = hq / hkv;
+  if (G > 64 || (G & (G - 1))) return PIE_ERR_INVALID;
+  if (static_cast<int64_t>(R) * a->max_pages_per_row >= (int64_t{1} << 31)) return PIE_ERR_RANGE;
+  if (R == 0) return PIE_OK;
+  if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->seq_lens || !a->out) return PIE_ERR_INVALID;
+  if (noalloc_layout(R, 1, hq, d).total > kNoAllocBytes) return PIE_ERR_RANGE;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PIE_ERR_CUDA;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return PIE_ERR_CUDA;
+      g_noalloc_addr[dev] = ptr;
+    }
+    base = g_noalloc_addr[dev];
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PIE_ERR_CUDA;
+
+  // KV splits: about 8 CTAs per SM over rows x splits x KV heads, lowered
+  // until the split partials fit in the array.
+  const int maxp = a->max_pages_per_row;
+  int S = static_cast<int>(std::min<int64_t>(maxp, std::max<int64_t>(1, (int64_t{sms} * 8 + int64_t{hkv} * R - 1) /
+                                                                              (int64_t{hkv} * R))));
+  while (S > 1 && noalloc_layout(R, S, hq, d).total > kNoAllocBytes) --S;
+  int chunk = (maxp + S - 1) / S;
+  S = (maxp + chunk - 1) / chunk;
+  const NoAllocLayout lay = noalloc_layout(R, S, hq, d);
+  if (lay.total > kNoAllocBytes) return PIE_ERR_RANGE;
+
+  uint8_t* sc = static_cast<uint8_t*>(base);
+  cudaStream_t st = static_cast<cudaStream_t>(a->stream);
+  WorkItem* items = reinterpret_cast<WorkItem*>(sc + lay.items);
+  int32_t* row_pos = reinterpret_cast<int32_t*>(sc + lay.row_pos);
+  int32_t* row_list = reinterpret_cast<int32_t*>(sc + lay.row_list);
+  int32_t* part_base = reinterpret_cast<int32_t*>(sc + lay.part_base);
+  int32_t* merge_rows = reinterpret_cast<int32_t*>(sc + lay.merge_rows);
+  int32_t* merge_np = reinterpret_cast<int32_t*>(sc + lay.merge_np);
+  float* acc = reinterpret_cast<float*>(sc + lay.acc);
+  float* ml = reinterpret_cast<float*>(sc + lay.ml);
+
+  const int n_items = R * S;
+  noalloc_plan<<<(n_items + 255) / 256, 256, 0, st>>>(R, S, chunk, maxp, a->seq_lens, items, row_pos, row_list,
+                                                       part_base, merge_rows, merge_np);
+  if (cudaGetLastError() != cudaSuccess) return PIE_ERR_CUDA;
+
+  Geometry g{a->num_layers, hq, hkv, d, a->num_pages, 0, static_cast<int64_t>(kPageSize) * d * 2};
+  PlanView v{};
+  v.page_ids = a->block_table;
+  v.row_pos = row_pos;
+  v.row_slot = nullptr;
+  v.row_part_base = part_base;
+  v.row_list = row_list;
+  v.dec_items = items;
+  v.pre_items = nullptr;
+  v.merge_rows = merge_rows;
+  v.merge_nparts = merge_np;
+  v.copies = nullptr;
+  v.n_rows = R;
+  v.n_dec = n_items;
+  v.n_pre = 0;
+  v.n_merge = S > 1 ? R : 0;
+  v.n_copies = 0;
+  cudaError_t e = d == 128 ? launch_decode_t<false, 128>(g, v, a->layer, a->q, a->k_pool, a->v_pool, nullptr, nullptr,
+                                                         a->out, a->lse, acc, ml, nullptr, st)
+                           : launch_decode_t<false, 64>(g, v, a->layer, a->q, a->k_pool, a->v_pool, nullptr, nullptr,
+                                                        a->out, a->lse, acc, ml, nullptr, st);
+  if (e == cudaSuccess && S > 1) e = launch_merge(g, v, a->out, a->lse, acc, ml, st);
+  return e == cudaSuccess ? PIE_OK : PIE_ERR_CUDA;
+}

@@ -29,8 +29,9 @@ EXPORTS = [
     "pie_ws_fork", "pie_ws_freeze", "pie_ws_rollback", "pie_ws_match_prefix", "pie_ws_info",
     "pie_ws_page_table", "pie_page_refcount", "pie_free_pages", "pie_batch_begin", "pie_batch_rows",
     "pie_batch_slots", "pie_kv_append", "pie_attend", "pie_batch_end", "pie_batch_plan_info",
-    "pie_batch_items", "pie_ctx_check",
+    "pie_batch_items", "pie_ctx_check", "pie_attend_decode_noalloc",
 ]
+PIE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class PieError(RuntimeError):
@@ -47,6 +48,17 @@ class pie_config(ctypes.Structure):
         ("free_list", ctypes.POINTER(ctypes.c_int32)),
         ("k_scale", ctypes.POINTER(ctypes.c_float)), ("v_scale", ctypes.POINTER(ctypes.c_float)),
         ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("stream", ctypes.c_void_p),
+    ]
+
+
+class pie_decode_args(ctypes.Structure):
+    _fields_ = [
+        ("num_rows", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("num_layers", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("layer", ctypes.c_int32), ("max_pages_per_row", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("stream", ctypes.c_void_p),
     ]
 
 
@@ -81,6 +93,7 @@ def _load():
         "pie_batch_plan_info": [V, P(I)],
         "pie_batch_items": [V, I, P(I), I, P(I)],
         "pie_ctx_check": [V, P(I)],
+        "pie_attend_decode_noalloc": [P(pie_decode_args)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -271,3 +284,17 @@ def pie_attend(ctx, batch, layer, q, out, lse=None) -> None:
 
 def pie_batch_end(ctx, batch) -> None:
     _check(ctx, lib.pie_batch_end(ctx, batch), "pie_batch_end")
+
+
+def pie_attend_decode_noalloc(num_rows, num_q_heads, num_kv_heads, head_dim, num_layers, num_pages, layer,
+                              max_pages_per_row, q, k_pool, v_pool, block_table, seq_lens, out, lse=None,
+                              stream=None) -> None:
+    """Decode attention with no device allocation (scratch in a library-owned
+    file-scope device array); see pie_attn.h."""
+    a = pie_decode_args()
+    a.num_rows, a.num_q_heads, a.num_kv_heads, a.head_dim = num_rows, num_q_heads, num_kv_heads, head_dim
+    a.num_layers, a.num_pages, a.layer, a.max_pages_per_row = num_layers, num_pages, layer, max_pages_per_row
+    a.q, a.k_pool, a.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
+    a.block_table, a.seq_lens = _ptr(block_table), _ptr(seq_lens)
+    a.out, a.lse, a.stream = _ptr(out), _ptr(lse), _ptr(stream)
+    _check(None, lib.pie_attend_decode_noalloc(ctypes.byref(a)), "pie_attend_decode_noalloc")
