@@ -321,24 +321,28 @@ class KVStore:
 
     def kv_append(self, pas: Pass, layer: int, k_bits: np.ndarray, v_bits: np.ndarray) -> None:
         """ops.attn.kv_append: write row r's K and V at its reserved slot."""
+        slots = np.asarray(pas.rows_slot, dtype=np.int64)
+        if slots.size == 0:
+            return
+        pages, s = slots // self.S, slots % self.S
         for kv, x in ((0, k_bits), (1, v_bits)):
-            data = self._encode(x, layer, kv)
-            for r, slot in enumerate(pas.rows_slot):
-                page, s = divmod(slot, self.S)
-                for h in range(self.Hkv):
-                    self.pool[kv, layer, page, h, self.offsets[s]] = data[r, h]
+            data = self._encode(x, layer, kv)                  # [n, Hkv, bytes]
+            for h in range(self.Hkv):
+                # row r's bytes go to offsets[s_r] of block (layer, page_r, h)
+                self.pool[kv, layer, pages[:, None], h, self.offsets[s]] = data[:, h, :]
 
     def read_kv(self, h: int, layer: int, upto: int):
         """Contiguous K, V [upto, Hkv, d] float64 of working set h's first tokens."""
         w = self._get(h)
+        pos = np.arange(upto)
+        pages = np.asarray(w.pages, dtype=np.int64)[pos // self.S]
+        offs = self.offsets[pos % self.S]                       # [upto, bytes]
         out = []
         for kv in (0, 1):
-            raw = np.empty((upto, self.Hkv, self.d * self.esize), dtype=np.uint8)
-            for pos in range(upto):
-                page = w.pages[pos // self.S]
-                raw[pos] = self.pool[kv, layer, page][:, self.offsets[pos % self.S]]
+            # raw[p, h, b] = pool[kv, layer, page(p), h, offs[p, b]]
+            raw = self.pool[kv, layer][pages[:, None, None], np.arange(self.Hkv)[None, :, None], offs[:, None, :]]
             if self.kv_dtype == KV_BF16:
-                vals = bf16_bits_to_f64(raw.view("<u2"))
+                vals = bf16_bits_to_f64(np.ascontiguousarray(raw).view("<u2"))
             else:
                 scale = (self.k_scale if kv == 0 else self.v_scale)[layer]
                 vals = np.stack([e4m3.dequantize(raw[:, hh, :], float(scale[hh]))

@@ -194,7 +194,11 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
   // fork / dedup groups: segments whose tables start with the same page
   std::unordered_map<int32_t, std::vector<int32_t>> by_first;
   std::vector<int32_t> first_order;
+  // Only decode-like segments (few rows) join a group: a prefill chunk reads
+  // its whole context itself, tile by tile, and sharing would only add
+  // partial results for each of its many rows.
   for (size_t i = 0; i < segs.size(); ++i) {
+    if (static_cast<int64_t>(segs[i].n_new) * G > kDecodeMaxM) continue;
     int32_t p0 = pb.page_ids[segs[i].table_off];
     auto& v = by_first[p0];
     if (v.empty()) first_order.push_back(p0);

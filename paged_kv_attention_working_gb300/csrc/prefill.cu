@@ -46,8 +46,8 @@ struct PreCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kQTile;
   static constexpr int kOffP = kOffKV + kStages * 2 * kKVTile;
-  static constexpr int kOffBar = kOffP + 2 * kPTile;
-  static constexpr int kNumBars = 2 * kStages + 4 + 4 + 2 + 2;
+  static constexpr int kOffBar = kOffP + 4 * kPTile;  // P: [tile][buffer]
+  static constexpr int kNumBars = 2 * kStages + 4 * 4;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;  // O tiles after 4 S buffers of 64 columns
@@ -72,10 +72,10 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + C::kStages;
-  uint64_t* s_full = bars + 2 * C::kStages;  // [tile][buf]
+  uint64_t* s_full = bars + 2 * C::kStages;  // [tile][buffer], S in tensor memory
   uint64_t* s_free = s_full + 4;
-  uint64_t* p_full = s_free + 4;             // [tile]
-  uint64_t* o_done = p_full + 2;
+  uint64_t* p_full = s_free + 4;             // [tile][buffer], P in shared memory
+  uint64_t* o_done = p_full + 4;             // [tile][buffer]: PV that read that P buffer is done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const WorkItem it = p.pre_items[blockIdx.x];
@@ -94,8 +94,6 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     for (int i = 0; i < 4; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
@@ -185,15 +183,16 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         const int s = j % C::kStages;
         const uint32_t vaddr = sbase + C::kOffKV + s * 2 * C::kKVTile + C::kKVTile;
         for (int t = 0; t < n_qt && ok; ++t) {
-          ok = mbar_wait(&p_full[t], j & 1, err);
+          const int b = j & 1;
+          ok = mbar_wait(&p_full[2 * t + b], (j >> 1) & 1, err);
           tc::fence_after();
-          const uint32_t paddr = sbase + C::kOffP + t * C::kPTile;
+          const uint32_t paddr = sbase + C::kOffP + (2 * t + b) * C::kPTile;
           const uint32_t d_o = tmem + C::kColO + t * D;
 #pragma unroll
           for (int ks = 0; ks < C::kKeys / 16; ++ks)
             tc::mma_bf16(d_o, tc::sw128_desc(paddr + ks * 32, 16, 1024),
                          tc::sw128_desc(vaddr + ks * 2048, C::kKeys * 128, 1024), id_o, j > 0 || ks > 0);
-          tc::commit(&o_done[t]);
+          tc::commit(&o_done[2 * t + b]);
         }
         tc::commit(&kv_empty[s]);
       }
@@ -213,7 +212,6 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     }
     const float qk_scale = 1.4426950408889634f * rsqrtf(static_cast<float>(D));
     float m_run = -INFINITY, l_run = 0.f;
-    uint8_t* prow = smem + C::kOffP + t * C::kPTile + r * 128;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
       const int b = j & 1;
@@ -228,7 +226,9 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[2 * t + b]);
 
-      const int lim = pos - (it.key_base + C::kKeys * j);  // columns <= lim are visible
+      // columns <= lim are visible: causal, and inside the item's key run
+      // (the tile past the run's end holds stand-in pages)
+      const int lim = min(pos - (it.key_base + C::kKeys * j), it.n_keys - 1 - C::kKeys * j);
       float f[64];
       float mx = -INFINITY;
 #pragma unroll
@@ -254,11 +254,18 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         pk[c] = pack_bf16(e0, e1);
       }
       l_run = l_run * alpha + sum;
-      if (j > 0) {
-        ok = warp_wait(&o_done[t], (j - 1) & 1, err);
-        if (!ok) break;
-        tc::fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
+      // P buffer b is free once PV(j-2) is done; a rescale of O needs every
+      // PV so far (up to j-1) done -- commits complete in issue order.
+      const bool any_resc = j > 0 && __any_sync(0xffffffffu, resc);
+      if (any_resc) {
+        ok = warp_wait(&o_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1, err);
+      } else if (j >= 2) {
+        ok = warp_wait(&o_done[2 * t + b], ((j - 2) >> 1) & 1, err);
+      }
+      if (!ok) break;
+      tc::fence_after();
+      if (any_resc) {
+        {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
@@ -272,6 +279,7 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
           tc::wait_st();
         }
       }
+      uint8_t* prow = smem + C::kOffP + (2 * t + b) * C::kPTile + r * 128;
 #pragma unroll
       for (int c16 = 0; c16 < 8; ++c16)
         *reinterpret_cast<uint4*>(prow + ((c16 ^ (r & 7)) << 4)) =
@@ -279,9 +287,9 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
       tc::fence_proxy_async_smem();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
+      if (lane == 0) mbar_arrive(&p_full[2 * t + b]);
     }
-    if (ok) ok = warp_wait(&o_done[t], (nkv - 1) & 1, err);
+    if (ok) ok = warp_wait(&o_done[2 * t + ((nkv - 1) & 1)], ((nkv - 1) >> 1) & 1, err);
     tc::fence_after();
     if (ok) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;

@@ -327,7 +327,7 @@ def reduced(name: str) -> Workload:
         return decode_batch(name="llama8b_decode_small", seed=12, n_ws=6, ctx_lo=200, ctx_hi=1500,
                             num_layers=2)
     if name == "fork_spec":
-        return fork_spec(name="fork_spec_small", seed=13, prompt=520, n_forks=5, suffix_hi=40)
+        return fork_spec(name="fork_spec_small", seed=13, prompt=600, n_forks=10, suffix_hi=40)
     if name == "mixed_batch":
         return mixed_batch(name="mixed_batch_small", seed=14, n_chunks=3, chunk_lo=100, chunk_hi=300,
                            ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400)

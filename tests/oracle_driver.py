@@ -15,11 +15,14 @@ def make_store(w, with_pool=True, page_size=None, free_list="seeded"):
                            k_scale=ks, v_scale=vs, with_pool=with_pool)
 
 
-def run(w, layers=None, with_pool=True, compute=True, store=None, on_pass=None):
+def run(w, layers=None, with_pool=True, compute=True, store=None, on_pass=None, kv_layers=None):
     """Execute every op.  Returns (store, handles, passes) where passes is a
-    list of dicts {segs, pass, out[layer], lse[layer]} for attending passes."""
+    list of dicts {segs, pass, out[layer], lse[layer]} for attending passes.
+    layers: layers attended (default all); kv_layers: layers whose K/V are
+    appended (default all)."""
     store = store or make_store(w, with_pool=with_pool)
     layers = range(w.num_layers) if layers is None else layers
+    kv_layers = range(w.num_layers) if kv_layers is None else kv_layers
     handles = {}
     passes = []
     for op in w.ops:
@@ -41,7 +44,7 @@ def run(w, layers=None, with_pool=True, compute=True, store=None, on_pass=None):
             pas = store.begin([(handles[s[0]], s[1], w.gather_tok(s[4])) for s in segs])
             rec = {"segs": segs, "pass": pas, "out": {}, "lse": {}}
             if with_pool:
-                for layer in (range(w.num_layers) if compute else ()):
+                for layer in (kv_layers if compute else ()):
                     k, v, q = w.pass_inputs(segs, layer, attend and layer in layers)
                     store.kv_append(pas, layer, k, v)
                     if attend and layer in layers:

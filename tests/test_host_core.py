@@ -262,3 +262,14 @@ def test_invalid_configurations_rejected():
         pie.pie_ctx_create(1, 4, 2, 128, 8, kv_dtype=pie.PIE_KV_E4M3)   # e4m3 without scales
     with pytest.raises(pie.PieError):
         pie.pie_ctx_create(1, 4, 2, 64, 4, free_list=[0, 1, 1, 2])      # not a permutation
+
+
+def test_plan_prefill_chunks_never_join_groups():
+    """A pass that appends long chunks to sets sharing a prefix plans every
+    row with one part (no partial results to merge)."""
+    w = wl.llama70b_fp8(n_ws=16, ctx_lo=2048, ctx_hi=4096, prefix_groups=2)
+    c, hs, b = _run_plan(w, 1)          # the fill pass after match_prefix
+    info = pie.pie_batch_plan_info(b)
+    assert info["merge_rows"] == 0 and info["prefill_items"] > 0
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
