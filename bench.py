@@ -233,22 +233,33 @@ def run_gpu(args, w, world, rank, local):
     ks, vs = w.scales()
     ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
                              k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
-    names = [f"w{i}" for i in range(len(w.ctx))]
-    hs = {n: pie.pie_ws_create(ctx) for n in names}
-    # fill the contexts: one pass, random bf16 K/V per layer generated on the device
+    # set-up: every operation of the workload before its final (decode) pass,
+    # with random bf16 K/V generated on the device
     gen = torch.Generator(device=dev)
     gen.manual_seed(1000 + rank)
-    b = pie.pie_batch_begin(ctx, [(hs[n], c, None) for n, c in zip(names, w.ctx)])
-    n_fill = pie.pie_batch_rows(b)
-    for layer in range(L):
-        k = torch.randn((n_fill, Hkv, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-        v = torch.randn((n_fill, Hkv, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-        pie.pie_kv_append(ctx, b, layer, k, v)
-        del k, v
-    pie.pie_batch_end(ctx, b)
-    for n in names:
-        pie.pie_ws_freeze(ctx, hs[n], -1)
+    hs = {}
+    last_pass = max(i for i, op in enumerate(w.ops) if op[0] == "pass")
+    for op in w.ops[:last_pass]:
+        kind = op[0]
+        if kind == "create":
+            hs[op[1]] = pie.pie_ws_create(ctx)
+        elif kind == "freeze":
+            pie.pie_ws_freeze(ctx, hs[op[1]], op[2])
+        elif kind == "match":
+            pie.pie_ws_match_prefix(ctx, hs[op[1]], w.tok_stream(op[2]).tolist())
+        elif kind == "pass":
+            b = pie.pie_batch_begin(ctx, [(hs[sg[0]], sg[1], w.gather_tok(sg[4])) for sg in op[1]])
+            n_fill = pie.pie_batch_rows(b)
+            for layer in range(L):
+                k = torch.randn((n_fill, Hkv, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                v = torch.randn((n_fill, Hkv, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                pie.pie_kv_append(ctx, b, layer, k, v)
+                del k, v
+            pie.pie_batch_end(ctx, b)
+        else:
+            raise ValueError(kind)
     torch.cuda.synchronize(dev)
+    names = [sg[0] for sg in w.ops[last_pass][1]]
     n_rows = len(names)
     q = torch.randn((L, n_rows, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
     kn = torch.randn((L, n_rows, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
@@ -257,9 +268,11 @@ def run_gpu(args, w, world, rank, local):
     lse = torch.empty((L, n_rows, Hq), dtype=torch.float32, device=dev)
     segs = [(hs[n], 1, None) for n in names]
 
-    # algorithmic bytes of one attend launch (one layer): every visible key once
-    keys = sum(c + 1 for c in w.ctx)
-    pages = sum(-(-(c + 1) // 16) for c in w.ctx)
+    # algorithmic bytes of one attend launch (one layer): every visible key
+    # once per working set, and pages shared by a dedup group once per group
+    shared = getattr(w, "shared_keys", 0)
+    keys = sum(c + 1 for c in w.ctx) - shared
+    pages = sum(-(-(c + 1) // 16) for c in w.ctx) - shared // 16
     kv_bytes_layer = keys * Hkv * D * esize * 2
     attend_bytes = kv_bytes_layer + 2 * n_rows * Hq * D * 2 + n_rows * Hq * 4 + 4 * pages
     append_bytes = n_rows * Hkv * D * (2 + esize) * 2
@@ -341,8 +354,10 @@ def run_gpu(args, w, world, rank, local):
     result = {
         "metric": "decode attend KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "n_ws": n_rows, "contexts": "uniform [512, 8192] seeded", "layers": L,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == 0 else "e4m3 KV, bf16 Q/O",
+        "data": "synthetic",
+        "config": {"workload": w.name, "n_ws": n_rows, "contexts": "uniform [%d, %d] seeded" % w.ctx_range,
+                   "layers": L,
                    "hq": Hq, "hkv": Hkv, "head_dim": D, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
                    "page_size": 16, "l2": "inputs larger than L2 (~1.1 GB KV per layer)",
                    "parallelism": f"replicas x{world}"},
@@ -465,7 +480,10 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=20.0,
                     help="CPU seconds of oracle work (whole reference run, or the cpu_baseline sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="llama8b_decode", choices=["llama8b_decode", "mixed_batch"])
+    ap.add_argument("--workload", default="llama8b_decode",
+                    choices=["llama8b_decode", "mixed_batch", "llama70b_fp8"])
+    ap.add_argument("--n-ws", type=int, default=0,
+                    help="working sets of the e4m3 workload (0 = the full 256; fewer only for profiling)")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
     args = ap.parse_args()
@@ -477,7 +495,13 @@ def main():
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
-    w = wl.llama8b_decode(num_layers=args.layers)
+    if args.workload == "llama70b_fp8":
+        n_ws = args.n_ws or 256
+        w = wl.llama70b_fp8(n_ws=n_ws, prefix_groups=n_ws // 8)
+        # keys of the shared dedup prefix beyond their first copy in each group
+        w.shared_keys = (n_ws - n_ws // 8) * 2048
+    else:
+        w = wl.llama8b_decode(num_layers=args.layers)
     if args.impl == "reference":
         run_reference(args, w, world, rank)
         return

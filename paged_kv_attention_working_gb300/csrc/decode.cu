@@ -16,8 +16,8 @@
 // makes a fork group's shared pages cost one read per group ("How Pie
 // thinks", section 4: the prompt is computed once and shared).
 //
-// E4M3 pages are converted in registers to f16 scaled by 2^-8 (an exact bit
-// move) and the scales are folded into the softmax and output scaling.
+// E4M3 pages are converted in registers to f16 (exact) and the per-head
+// scales are folded into the softmax and output scaling.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -102,8 +102,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Geometry g, PlanView p
   // -------------------------------------------------------------- consumers
   const int mt = warp % n_mt, grp = warp / n_mt;
   const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group / thread in quad
-  const float kdq = E4M3 ? kscale[layer * g.hkv + head] * 256.0f : 1.0f;
-  const float vdq = E4M3 ? vscale[layer * g.hkv + head] * 256.0f : 1.0f;
+  const float kdq = E4M3 ? kscale[layer * g.hkv + head] : 1.0f;
+  const float vdq = E4M3 ? vscale[layer * g.hkv + head] : 1.0f;
   const float qk_scale = kdq * rsqrtf(static_cast<float>(D)) * 1.4426950408889634f;
 
   // the two M rows this thread holds: m = 16*mt + gq (+8)
@@ -183,14 +183,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Geometry g, PlanView p
         uint32_t addr = kb + key * 128 + 16 * (c ^ (key & 7));
         uint32_t r0, r1, r2, r3;  // (keys 0-7, chunk 2kp) (0-7, 2kp+1) (8-15, 2kp) (8-15, 2kp+1)
         ldsm_x4(addr, r0, r1, r2, r3);
-        mma16816<false>(sc[0], qa[2 * kp], e4m3x2_to_f16x2_scaled(prmt(r0, 0, 0x1404)),
-                        e4m3x2_to_f16x2_scaled(prmt(r0, 0, 0x3424)));
-        mma16816<false>(sc[1], qa[2 * kp], e4m3x2_to_f16x2_scaled(prmt(r2, 0, 0x1404)),
-                        e4m3x2_to_f16x2_scaled(prmt(r2, 0, 0x3424)));
-        mma16816<false>(sc[0], qa[2 * kp + 1], e4m3x2_to_f16x2_scaled(prmt(r1, 0, 0x1404)),
-                        e4m3x2_to_f16x2_scaled(prmt(r1, 0, 0x3424)));
-        mma16816<false>(sc[1], qa[2 * kp + 1], e4m3x2_to_f16x2_scaled(prmt(r3, 0, 0x1404)),
-                        e4m3x2_to_f16x2_scaled(prmt(r3, 0, 0x3424)));
+        // bytes 4t, 4t+1 -> k-slots 2t, 2t+1; bytes 4t+2, 4t+3 -> k-slots 2t+8, 2t+9
+        mma16816<false>(sc[0], qa[2 * kp], e4m3x2_lo_to_f16x2(r0), e4m3x2_hi_to_f16x2(r0));
+        mma16816<false>(sc[1], qa[2 * kp], e4m3x2_lo_to_f16x2(r2), e4m3x2_hi_to_f16x2(r2));
+        mma16816<false>(sc[0], qa[2 * kp + 1], e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r1));
+        mma16816<false>(sc[1], qa[2 * kp + 1], e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r3));
       }
     }
 
@@ -211,17 +208,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Geometry g, PlanView p
         }
       best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
       best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
-      float mnew = fmaxf(mx[h], best);
-      float base = mnew == -INFINITY ? 0.f : mnew;
-      float alpha = ex2(mx[h] - base);
-      mx[h] = mnew;
+      // The reference max only moves when the row max exceeds it by more
+      // than 8 (log2 units): weights stay <= 2^8, and O is rescaled rarely.
+      const bool up = best > mx[h] + 8.f;
+      const float mnew = up ? best : mx[h];
+      const float base = mnew == -INFINITY ? 0.f : mnew;
       pm[h] = base;
-      sum[h] *= alpha;
+      if (__any_sync(0xffffffffu, up)) {
+        const float alpha = up ? ex2(mx[h] - base) : 1.f;
+        sum[h] *= alpha;
 #pragma unroll
-      for (int i = 0; i < C::kNT; ++i) {
-        o[i][2 * h] *= alpha;
-        o[i][2 * h + 1] *= alpha;
+        for (int i = 0; i < C::kNT; ++i) {
+          o[i][2 * h] *= alpha;
+          o[i][2 * h + 1] *= alpha;
+        }
       }
+      mx[h] = mnew;
     }
     uint32_t pa[4];
 #pragma unroll
@@ -258,11 +260,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Geometry g, PlanView p
           w[jj] = lds32(vb + key * 128 + 16 * (c ^ (key & 7)) + 4 * (gq & 3));
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t sel = i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12);
-          uint32_t b0 = e4m3x2_to_f16x2_scaled(prmt(w[0], w[1], sel));
-          uint32_t b1 = e4m3x2_to_f16x2_scaled(prmt(w[2], w[3], sel));
-          mma16816<false>(o[4 * mq + i], pa, b0, b1);
+        for (int i = 0; i < 4; i += 2) {
+          // bytes: (key 2t, d_i) (key 2t+1, d_i) (key 2t, d_i+1) (key 2t+1, d_i+1), same for keys 2t+8, 2t+9
+          const uint32_t sel = i | ((4 + i) << 4) | ((i + 1) << 8) | ((5 + i) << 12);
+          const uint32_t x01 = prmt(w[0], w[1], sel), x23 = prmt(w[2], w[3], sel);
+          mma16816<false>(o[4 * mq + i], pa, e4m3x2_lo_to_f16x2(x01), e4m3x2_lo_to_f16x2(x23));
+          mma16816<false>(o[4 * mq + i + 1], pa, e4m3x2_hi_to_f16x2(x01), e4m3x2_hi_to_f16x2(x23));
         }
       }
     }

@@ -152,40 +152,51 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     }
   } else if (warp == 8) {
     // ----------------------------------------------------------------- MMA
+    // One thread issues everything, event-driven: S(j) for both Q tiles as
+    // soon as K tile j has landed and both S buffers of parity j are free,
+    // PV(j) of a Q tile as soon as its P(j) is written; K/V stage j is
+    // released right after the last PV(j).  Nothing waits on a later tile
+    // to release an earlier one.
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_bf16(128, C::kKeys, false, false);
       const uint32_t id_o = tc::idesc_bf16(128, D, false, true);
-      bool ok = true;
-      auto issue_s = [&](int j) {
-        const int s = j % C::kStages;
-        ok = ok && mbar_wait(&kv_full[s], (j / C::kStages) & 1, err);
-        tc::fence_after();
-        const uint32_t kaddr = sbase + C::kOffKV + s * 2 * C::kKVTile;
-        for (int t = 0; t < n_qt && ok; ++t) {
-          const int b = j & 1;
-          if (j >= 2) ok = mbar_wait(&s_free[2 * t + b], ((j >> 1) - 1) & 1, err);
-          tc::fence_after();
-          const uint32_t d_s = tmem + (2 * t + b) * C::kKeys;
-          const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
+      int s_next = 0;
+      int pv_next[2] = {0, n_qt > 1 ? 0 : nkv};
+      uint32_t idle = 0;
+      while ((pv_next[0] < nkv || pv_next[1] < nkv) && idle < kWaitLimit) {
+        bool progressed = false;
+        if (s_next < nkv) {
+          const int j = s_next, st = j % C::kStages, b = j & 1;
+          bool ready = mbar_test_wait(&kv_full[st], (j / C::kStages) & 1);
+          for (int t = 0; t < n_qt && ready && j >= 2; ++t)
+            ready = mbar_test_wait(&s_free[2 * t + b], ((j >> 1) - 1) & 1);
+          if (ready) {
+            tc::fence_after();
+            const uint32_t kaddr = sbase + C::kOffKV + st * 2 * C::kKVTile;
+            for (int t = 0; t < n_qt; ++t) {
+              const uint32_t d_s = tmem + (2 * t + b) * C::kKeys;
+              const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off_q = (ks >> 2) * 16384 + (ks & 3) * 32;
-            const uint32_t off_k = (ks >> 2) * (C::kKeys * 128) + (ks & 3) * 32;
-            tc::mma_bf16(d_s, tc::sw128_desc(qaddr + off_q, 16, 1024), tc::sw128_desc(kaddr + off_k, 16, 1024), id_s,
-                         ks > 0);
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off_q = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint32_t off_k = (ks >> 2) * (C::kKeys * 128) + (ks & 3) * 32;
+                tc::mma_bf16(d_s, tc::sw128_desc(qaddr + off_q, 16, 1024),
+                             tc::sw128_desc(kaddr + off_k, 16, 1024), id_s, ks > 0);
+              }
+              tc::commit(&s_full[2 * t + b]);
+            }
+            ++s_next;
+            progressed = true;
           }
-          tc::commit(&s_full[2 * t + b]);
         }
-      };
-      issue_s(0);
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (j + 1 < nkv) issue_s(j + 1);
-        const int s = j % C::kStages;
-        const uint32_t vaddr = sbase + C::kOffKV + s * 2 * C::kKVTile + C::kKVTile;
-        for (int t = 0; t < n_qt && ok; ++t) {
+        for (int t = 0; t < n_qt; ++t) {
+          const int j = pv_next[t];
+          if (j >= s_next) continue;  // S(j) not issued yet (nor P(j) written)
           const int b = j & 1;
-          ok = mbar_wait(&p_full[2 * t + b], (j >> 1) & 1, err);
+          if (!mbar_test_wait(&p_full[2 * t + b], (j >> 1) & 1)) continue;
           tc::fence_after();
+          const int st = j % C::kStages;
+          const uint32_t vaddr = sbase + C::kOffKV + st * 2 * C::kKVTile + C::kKVTile;
           const uint32_t paddr = sbase + C::kOffP + (2 * t + b) * C::kPTile;
           const uint32_t d_o = tmem + C::kColO + t * D;
 #pragma unroll
@@ -193,9 +204,16 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
             tc::mma_bf16(d_o, tc::sw128_desc(paddr + ks * 32, 16, 1024),
                          tc::sw128_desc(vaddr + ks * 2048, C::kKeys * 128, 1024), id_o, j > 0 || ks > 0);
           tc::commit(&o_done[2 * t + b]);
+          pv_next[t] = j + 1;
+          progressed = true;
+          // the stage is free once both tiles' PV(j) are issued (commit
+          // arrives after every MMA issued so far has completed)
+          const int other = n_qt > 1 ? pv_next[1 - t] : nkv;
+          if (other > j) tc::commit(&kv_empty[st]);
         }
-        tc::commit(&kv_empty[s]);
+        idle = progressed ? 0 : idle + 1;
       }
+      if (idle >= kWaitLimit && err) atomicOr(err, kErrWaitTimeout);
     }
     __syncwarp();
   } else if (warp / 4 < n_qt) {
@@ -230,12 +248,23 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
       // (the tile past the run's end holds stand-in pages)
       const int lim = min(pos - (it.key_base + C::kKeys * j), it.n_keys - 1 - C::kKeys * j);
       float f[64];
-      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        f[c] = c <= lim ? __uint_as_float(sr[c]) * qk_scale : -INFINITY;
-        mx = fmaxf(mx, f[c]);
+      for (int c = 0; c < 64; ++c) f[c] = __uint_as_float(sr[c]);
+      if (!__all_sync(0xffffffffu, lim >= 63)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) f[c] = c <= lim ? f[c] : -INFINITY;
       }
+      // row max with 8 independent chains (scale > 0, so the max commutes with it)
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = f[i];
+#pragma unroll
+      for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], f[c]);
+#pragma unroll
+      for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < w2; ++i) m8[i] = fmaxf(m8[i], m8[i + w2]);
+      const float mx = m8[0] * qk_scale;
       float alpha = 1.f;
       bool resc = false;
       const float m_new = fmaxf(m_run, mx);
@@ -244,15 +273,23 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         m_run = m_new;
         resc = true;
       }
-      const float base = m_run == -INFINITY ? 0.f : m_run;
-      float sum = 0.f;
+      const float nb = m_run == -INFINITY ? 0.f : -m_run;
+      float s8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s8[i] = 0.f;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        float e0 = ex2(f[2 * c] - base), e1 = ex2(f[2 * c + 1] - base);
-        sum += e0 + e1;
+        const float e0 = ex2(fmaf(f[2 * c], qk_scale, nb)), e1 = ex2(fmaf(f[2 * c + 1], qk_scale, nb));
+        s8[(2 * c) & 7] += e0;
+        s8[(2 * c + 1) & 7] += e1;
         pk[c] = pack_bf16(e0, e1);
       }
+#pragma unroll
+      for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < w2; ++i) s8[i] += s8[i + w2];
+      const float sum = s8[0];
       l_run = l_run * alpha + sum;
       // P buffer b is free once PV(j-2) is done; a rescale of O needs every
       // PV so far (up to j-1) done -- commits complete in issue order.

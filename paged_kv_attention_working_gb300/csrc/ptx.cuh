@@ -45,6 +45,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: true when the phase completed, false after kWaitLimit polls
 // (then *err gets kErrWaitTimeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
@@ -124,13 +135,18 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
-// Two E4M3 bytes, placed in bits 8..15 and 24..31 of x, to two f16 values
-// equal to 2^-8 times the E4M3 values (exact for every finite code): the
-// E4M3 exponent and mantissa fields land in the f16 fields unchanged, so
-// the f16 exponent bias (15) is 8 above E4M3's (7); subnormals line up the
-// same way.  Bits 0..7 and 16..23 of x are ignored.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t x) {
-  return ((x >> 1) & 0x3F803F80u) | (x & 0x80008000u);
+// Two OCP FP8 E4M3 values (bits 0..7 and 8..15 of x, element 0 low) to
+// f16x2, exact (every finite E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}" : "=r"(r) : "r"(x));
+  return r;
+}
+// Same for bits 16..23 and 24..31.
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, hi;\n}" : "=r"(r) : "r"(x));
+  return r;
 }
 
 }  // namespace pie

@@ -204,6 +204,7 @@ def decode_batch(name="llama8b_decode", seed=2, n_ws=64, ctx_lo=512, ctx_hi=8192
         unique -= (n_ws - prefix_groups) * (prefix_len // 16)
     w.num_pages = unique + slack_pages
     w.ctx = ctx
+    w.ctx_range = (ctx_lo, ctx_hi)
     return w
 
 
