@@ -12,13 +12,17 @@
 //                   layout is exactly the 128-byte-swizzled K-major (K) and
 //                   MN-major (V) operand layout, so pages land ready for MMA;
 //   MMA warp        S_t = Q_t K^T   (tcgen05.mma M=128 N=64 K=16, fp32 in
-//                   tensor memory, double-buffered) for both Q tiles, then
-//                   O_t += P_t V    (M=128 N=d K=16, O in tensor memory);
+//                   tensor memory) for both Q tiles, then
+//                   O_t += P_t V    (M=128 N=d K=16, A operand P read from
+//                   tensor memory, O in tensor memory);
 //   softmax warps   one warpgroup per Q tile, one thread per row: loads its
-//                   S row from tensor memory, masks, keeps the running max
-//                   and sum, rescales O in tensor memory only when the max
-//                   grew by more than 2^8 (otherwise the stale max is kept),
-//                   writes P (bf16) to shared memory for the PV MMA.
+//                   S row from tensor memory (freeing S for the next tile at
+//                   once), masks, keeps the running max and sum, rescales O
+//                   in tensor memory only when the max grew by more than 2^8
+//                   (otherwise the stale max is kept), and writes P as bf16
+//                   pairs into one of two tensor-memory P buffers.
+// Tensor memory: S 2 x 64 columns, P 2 x 2 x 32, O 2 x d (512 in all); with
+// P there, shared memory holds Q and a 5-stage K/V ring.
 // Rows with one part are normalised and written as bf16; otherwise the
 // fp32 (acc, m, l) partial goes to the merge kernel.
 #include <cuda_bf16.h>
@@ -39,18 +43,18 @@ struct PreCfg {
   static constexpr int kPanels = D / 64;
   static constexpr int kKeys = 64;
   static constexpr int kPagesPerTile = kKeys / kPageSize;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = D == 128 ? 5 : 6;
   static constexpr int kQTile = 128 * D * 2;
   static constexpr int kKVTile = kKeys * D * 2;
-  static constexpr int kPTile = 128 * kKeys * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kQTile;
-  static constexpr int kOffP = kOffKV + kStages * 2 * kKVTile;
-  static constexpr int kOffBar = kOffP + 4 * kPTile;  // P: [tile][buffer]
-  static constexpr int kNumBars = 2 * kStages + 4 * 4;
+  static constexpr int kOffBar = kOffKV + kStages * 2 * kKVTile;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 4 + 4;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;  // O tiles after 4 S buffers of 64 columns
+  static constexpr uint32_t kColS = 0;    // S of tile t at t * 64
+  static constexpr uint32_t kColP = 128;  // P of tile t, buffer b at 128 + t * 64 + b * 32
+  static constexpr uint32_t kColO = 256;  // O of tile t at 256 + t * d
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err) {
@@ -72,10 +76,10 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + C::kStages;
-  uint64_t* s_full = bars + 2 * C::kStages;  // [tile][buffer], S in tensor memory
-  uint64_t* s_free = s_full + 4;
-  uint64_t* p_full = s_free + 4;             // [tile][buffer], P in shared memory
-  uint64_t* o_done = p_full + 4;             // [tile][buffer]: PV that read that P buffer is done
+  uint64_t* s_full = bars + 2 * C::kStages;  // [tile]: S(j) in tensor memory
+  uint64_t* s_free = s_full + 2;             // [tile]: S(j) loaded into registers
+  uint64_t* p_full = s_free + 2;             // [tile][buffer]: P(j) written
+  uint64_t* o_done = p_full + 4;             // [tile][buffer]: PV(j) that read P buffer b done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const WorkItem it = p.pre_items[blockIdx.x];
@@ -91,9 +95,11 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   } else if (warp == 8) {
     // ----------------------------------------------------------------- MMA
     // One thread issues everything, event-driven: S(j) for both Q tiles as
-    // soon as K tile j has landed and both S buffers of parity j are free,
+    // soon as K tile j has landed and both tiles' S(j-1) are in registers,
     // PV(j) of a Q tile as soon as its P(j) is written; K/V stage j is
     // released right after the last PV(j).  Nothing waits on a later tile
     // to release an earlier one.
@@ -168,13 +174,12 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         if (s_next < nkv) {
           const int j = s_next, st = j % C::kStages, b = j & 1;
           bool ready = mbar_test_wait(&kv_full[st], (j / C::kStages) & 1);
-          for (int t = 0; t < n_qt && ready && j >= 2; ++t)
-            ready = mbar_test_wait(&s_free[2 * t + b], ((j >> 1) - 1) & 1);
+          for (int t = 0; t < n_qt && ready && j > 0; ++t) ready = mbar_test_wait(&s_free[t], (j - 1) & 1);
           if (ready) {
             tc::fence_after();
             const uint32_t kaddr = sbase + C::kOffKV + st * 2 * C::kKVTile;
             for (int t = 0; t < n_qt; ++t) {
-              const uint32_t d_s = tmem + (2 * t + b) * C::kKeys;
+              const uint32_t d_s = tmem + C::kColS + t * C::kKeys;
               const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
 #pragma unroll
               for (int ks = 0; ks < D / 16; ++ks) {
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
                 tc::mma_bf16(d_s, tc::sw128_desc(qaddr + off_q, 16, 1024),
                              tc::sw128_desc(kaddr + off_k, 16, 1024), id_s, ks > 0);
               }
-              tc::commit(&s_full[2 * t + b]);
+              tc::commit(&s_full[t]);
             }
             ++s_next;
             progressed = true;
@@ -197,12 +202,12 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
           tc::fence_after();
           const int st = j % C::kStages;
           const uint32_t vaddr = sbase + C::kOffKV + st * 2 * C::kKVTile + C::kKVTile;
-          const uint32_t paddr = sbase + C::kOffP + (2 * t + b) * C::kPTile;
+          const uint32_t p_tmem = tmem + C::kColP + t * 64 + b * 32;  // 16 keys = 8 columns per k-step
           const uint32_t d_o = tmem + C::kColO + t * D;
 #pragma unroll
           for (int ks = 0; ks < C::kKeys / 16; ++ks)
-            tc::mma_bf16(d_o, tc::sw128_desc(paddr + ks * 32, 16, 1024),
-                         tc::sw128_desc(vaddr + ks * 2048, C::kKeys * 128, 1024), id_o, j > 0 || ks > 0);
+            tc::mma_bf16_ts(d_o, p_tmem + ks * 8, tc::sw128_desc(vaddr + ks * 2048, C::kKeys * 128, 1024), id_o,
+                            j > 0 || ks > 0);
           tc::commit(&o_done[2 * t + b]);
           pv_next[t] = j + 1;
           progressed = true;
@@ -233,16 +238,16 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
       const int b = j & 1;
-      ok = warp_wait(&s_full[2 * t + b], (j >> 1) & 1, err);
+      ok = warp_wait(&s_full[t], j & 1, err);
       if (!ok) break;
       tc::fence_after();
       uint32_t sr[64];
-      tc::ld32(tmem + lane_base + (2 * t + b) * C::kKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tc::ld32(tmem + lane_base + (2 * t + b) * C::kKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tc::ld32(tmem + lane_base + C::kColS + t * C::kKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tc::ld32(tmem + lane_base + C::kColS + t * C::kKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[2 * t + b]);
+      if (lane == 0) mbar_arrive(&s_free[t]);
 
       // columns <= lim are visible: causal, and inside the item's key run
       // (the tile past the run's end holds stand-in pages)
@@ -316,12 +321,9 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
           tc::wait_st();
         }
       }
-      uint8_t* prow = smem + C::kOffP + (2 * t + b) * C::kPTile + r * 128;
-#pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
-        *reinterpret_cast<uint4*>(prow + ((c16 ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      tc::fence_proxy_async_smem();
+      // P as bf16 pairs (key 2c in the low half of column c): the A operand of PV(j)
+      tc::st32(tmem + lane_base + C::kColP + t * 64 + b * 32, pk);
+      tc::wait_st();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[2 * t + b]);
