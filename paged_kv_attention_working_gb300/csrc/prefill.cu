@@ -4,25 +4,28 @@
 // frozen prefix of a fork group).
 //
 // One CTA takes one work item for one KV head: up to 256 query rows x query
-// heads of that KV group (M, in two 128-row tiles), which all read the same
-// run of pages, causally (key position <= row position).  Per 64-key tile
-// (4 pages):
-//   producer warp   16 one-dimensional bulk copies (K and V, 4 pages x 2
-//                   panels of 2 KB) into a 3-stage ring; the pool's block
-//                   layout is exactly the 128-byte-swizzled K-major (K) and
-//                   MN-major (V) operand layout, so pages land ready for MMA;
-//   MMA warp        S_t = Q_t K^T   (tcgen05.mma M=128 N=64 K=16, fp32 in
-//                   tensor memory) for both Q tiles, then
-//                   O_t += P_t V    (M=128 N=d K=16, A operand P read from
-//                   tensor memory, O in tensor memory);
+// heads of that KV group (M, in two 128-row tiles t = 0, 1), which all read
+// the same run of pages, causally (key position <= row position).  Keys go
+// in tiles of 128 (8 pages):
+//   producer warp   bulk copies of 2-KB page panels into a K ring and a V
+//                   ring (separate, so a K tile is refilled as soon as both
+//                   S products have read it); the pool's block layout is the
+//                   128-byte-swizzled operand layout, so pages land ready for
+//                   the tensor cores (K-major for K, MN-major for V);
+//   MMA thread      event-driven issue of S_t = Q_t K^T (tcgen05.mma M=128
+//                   N=128 K=16, fp32 in tensor memory) and O_t += P_t V
+//                   (M=128 N=d K=16, A = P read from tensor memory, O in
+//                   tensor memory); S_t(j+1) overwrites S_t(j) / P_t(j), so it
+//                   is issued once PV_t(j) has completed -- the two Q tiles
+//                   keep the tensor pipe busy in turn;
 //   softmax warps   one warpgroup per Q tile, one thread per row: loads its
-//                   S row from tensor memory (freeing S for the next tile at
-//                   once), masks, keeps the running max and sum, rescales O
-//                   in tensor memory only when the max grew by more than 2^8
-//                   (otherwise the stale max is kept), and writes P as bf16
-//                   pairs into one of two tensor-memory P buffers.
-// Tensor memory: S 2 x 64 columns, P 2 x 2 x 32, O 2 x d (512 in all); with
-// P there, shared memory holds Q and a 5-stage K/V ring.
+//                   128-score S row from tensor memory, takes the row max,
+//                   keeps the running max stale unless the row max grew by
+//                   more than 2^8 (then O is rescaled in tensor memory),
+//                   computes the weights with packed f32x2 arithmetic and
+//                   writes P back as bf16 pairs over the row's first 64 S
+//                   columns.
+// Tensor memory: S/P of tile t at columns t*128, O of tile t at 256 + t*d.
 // Rows with one part are normalised and written as bf16; otherwise the
 // fp32 (acc, m, l) partial goes to the merge kernel.
 #include <cuda_bf16.h>
@@ -36,26 +39,63 @@
 namespace pie {
 namespace {
 
-constexpr int kThreadsPre = 320;  // 8 softmax warps, MMA warp, producer warp
+constexpr int kThreadsPre = 320;  // 8 softmax warps, MMA warp 8, producer warp 9
 
 template <int D>
 struct PreCfg {
   static constexpr int kPanels = D / 64;
-  static constexpr int kKeys = 64;
-  static constexpr int kPagesPerTile = kKeys / kPageSize;
-  static constexpr int kStages = D == 128 ? 5 : 6;
+  static constexpr int kKeys = 128;                       // keys per tile
+  static constexpr int kPagesPerTile = kKeys / kPageSize;  // 8
   static constexpr int kQTile = 128 * D * 2;
-  static constexpr int kKVTile = kKeys * D * 2;
+  static constexpr int kKVTile = kKeys * D * 2;            // one K (or V) tile
+  static constexpr int kPanelBytes = kKeys * 128;          // one 64-column panel of a tile
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 3;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = 2 * kQTile;
-  static constexpr int kOffBar = kOffKV + kStages * 2 * kKVTile;
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 4 + 4;
+  static constexpr int kOffK = 2 * kQTile;
+  static constexpr int kOffV = kOffK + kKStages * kKVTile;
+  static constexpr int kOffBar = kOffV + kVStages * kKVTile;
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;    // S of tile t at t * 64
-  static constexpr uint32_t kColP = 128;  // P of tile t, buffer b at 128 + t * 64 + b * 32
-  static constexpr uint32_t kColO = 256;  // O of tile t at 256 + t * d
+  static constexpr uint32_t kColO = 256;
 };
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two softmax weights: e = 2^(s * scale + nb) for a pair of scores (one
+// packed f32x2 FMA, two ex2), added to a packed pair of running sums;
+// returns the pair as bf16x2 (element 0 low).
+__device__ __forceinline__ uint32_t softmax_pair(float s0, float s1, float scale, float nb, uint64_t& acc) {
+  uint32_t pk;
+  asm("{\n"
+      " .reg .b64 s, k, n, x, e;\n"
+      " .reg .f32 x0, x1, e0, e1;\n"
+      " mov.b64 s, {%2, %3};\n"
+      " mov.b64 k, {%4, %4};\n"
+      " mov.b64 n, {%5, %5};\n"
+      " fma.rn.f32x2 x, s, k, n;\n"
+      " mov.b64 {x0, x1}, x;\n"
+      " ex2.approx.ftz.f32 e0, x0;\n"
+      " ex2.approx.ftz.f32 e1, x1;\n"
+      " mov.b64 e, {e0, e1};\n"
+      " add.rn.f32x2 %1, %1, e;\n"
+      " cvt.rn.bf16x2.f32 %0, e1, e0;\n"
+      "}"
+      : "=r"(pk), "+l"(acc)
+      : "f"(s0), "f"(s1), "f"(scale), "f"(nb));
+  return pk;
+}
+
+__device__ __forceinline__ float sum_pair(uint64_t acc) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc));
+  return a + b;
+}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err) {
   bool ok = mbar_wait(bar, parity, err);
@@ -74,12 +114,13 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + C::kStages;
-  uint64_t* s_full = bars + 2 * C::kStages;  // [tile]: S(j) in tensor memory
-  uint64_t* s_free = s_full + 2;             // [tile]: S(j) loaded into registers
-  uint64_t* p_full = s_free + 2;             // [tile][buffer]: P(j) written
-  uint64_t* o_done = p_full + 4;             // [tile][buffer]: PV(j) that read P buffer b done
+  uint64_t* k_full = bars;                        // [K stage]
+  uint64_t* k_empty = k_full + C::kKStages;
+  uint64_t* v_full = k_empty + C::kKStages;       // [V stage]
+  uint64_t* v_empty = v_full + C::kVStages;
+  uint64_t* s_full = v_empty + C::kVStages;       // [tile]: S_t(j) in tensor memory
+  uint64_t* p_full = s_full + 2;                  // [tile]: P_t(j) written (and O rescaled)
+  uint64_t* o_done = p_full + 2;                  // [tile]: PV_t(j) complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const WorkItem it = p.pre_items[blockIdx.x];
@@ -91,17 +132,18 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&p_full[i], 4);
-      mbar_init(&o_done[i], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
     }
     fence_mbar_init();
   }
@@ -134,87 +176,104 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
+    // K(j) and V(j) each take one copy per lane: 8 pages x kPanels panels.
     const int64_t layer_blk = static_cast<int64_t>(layer) * g.num_pages * g.hkv;
-    constexpr int kCopies = C::kPagesPerTile * C::kPanels * 2;
-    bool ok = true;
-    for (int j = 0; j < nkv && ok; ++j) {
-      const int s = j % C::kStages;
-      if (j >= C::kStages) ok = warp_wait(&kv_empty[s], ((j / C::kStages) - 1) & 1, err);
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], 2 * C::kKVTile);
-      __syncwarp();
+    constexpr int kCopies = C::kPagesPerTile * C::kPanels;
+    int kn = 0, vn = 0;
+    uint32_t idle = 0;
+    while ((kn < nkv || vn < nkv) && idle < kWaitLimit) {
+      int which = -1;  // lane 0 decides: 0 = K(kn), 1 = V(vn)
+      if (lane == 0) {
+        if (kn < nkv && (kn < C::kKStages ||
+                         mbar_test_wait(&k_empty[kn % C::kKStages], ((kn / C::kKStages) - 1) & 1)))
+          which = 0;
+        else if (vn < kn && (vn < C::kVStages ||
+                             mbar_test_wait(&v_empty[vn % C::kVStages], ((vn / C::kVStages) - 1) & 1)))
+          which = 1;
+        if (which == 0) mbar_arrive_expect_tx(&k_full[kn % C::kKStages], C::kKVTile);
+        if (which == 1) mbar_arrive_expect_tx(&v_full[vn % C::kVStages], C::kKVTile);
+      }
+      which = __shfl_sync(0xffffffffu, which, 0);
+      if (which < 0) {
+        ++idle;
+        continue;
+      }
+      idle = 0;
+      const int j = which == 0 ? kn : vn;
       if (lane < kCopies) {
-        const int kv = lane / (C::kPagesPerTile * C::kPanels);
-        const int rem = lane % (C::kPagesPerTile * C::kPanels);
-        const int pg = rem / C::kPanels, panel = rem % C::kPanels;
+        const int pg = lane / C::kPanels, panel = lane % C::kPanels;
         int pj = C::kPagesPerTile * j + pg;
         if (pj >= it.n_pages) pj = it.n_pages - 1;  // keys there are masked; any finite page will do
         const int page = p.page_ids[it.pages_off + pj];
         const int64_t off = (layer_blk + static_cast<int64_t>(page) * g.hkv + head) * g.block_bytes + panel * 2048;
-        uint8_t* dst = smem + C::kOffKV + s * 2 * C::kKVTile + kv * C::kKVTile + panel * (C::kKeys * 128) + pg * 2048;
-        bulk_g2s(dst, (kv ? vpool : kpool) + off, 2048, &kv_full[s]);
+        if (which == 0) {
+          uint8_t* dst = smem + C::kOffK + (j % C::kKStages) * C::kKVTile + panel * C::kPanelBytes + pg * 2048;
+          bulk_g2s(dst, kpool + off, 2048, &k_full[j % C::kKStages]);
+        } else {
+          uint8_t* dst = smem + C::kOffV + (j % C::kVStages) * C::kKVTile + panel * C::kPanelBytes + pg * 2048;
+          bulk_g2s(dst, vpool + off, 2048, &v_full[j % C::kVStages]);
+        }
       }
+      if (which == 0)
+        ++kn;
+      else
+        ++vn;
       __syncwarp();
     }
+    if (idle >= kWaitLimit && lane == 0 && err) atomicOr(err, kErrWaitTimeout);
   } else if (warp == 8) {
     // ----------------------------------------------------------------- MMA
-    // One thread issues everything, event-driven: S(j) for both Q tiles as
-    // soon as K tile j has landed and both tiles' S(j-1) are in registers,
-    // PV(j) of a Q tile as soon as its P(j) is written; K/V stage j is
-    // released right after the last PV(j).  Nothing waits on a later tile
-    // to release an earlier one.
+    // One thread issues everything, event-driven, PVs first (they gate the
+    // next S of their tile): PV_t(j) once P_t(j) is written and V(j)
+    // landed; S_t(j) once K(j) landed and PV_t(j-1) is complete (S_t(j)
+    // overwrites P_t(j-1)).  A K (V) stage is released by a commit after the
+    // last S (PV) that reads it.
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_bf16(128, C::kKeys, false, false);
       const uint32_t id_o = tc::idesc_bf16(128, D, false, true);
-      int s_next = 0;
+      int s_next[2] = {0, n_qt > 1 ? 0 : nkv};
       int pv_next[2] = {0, n_qt > 1 ? 0 : nkv};
       uint32_t idle = 0;
       while ((pv_next[0] < nkv || pv_next[1] < nkv) && idle < kWaitLimit) {
         bool progressed = false;
-        if (s_next < nkv) {
-          const int j = s_next, st = j % C::kStages, b = j & 1;
-          bool ready = mbar_test_wait(&kv_full[st], (j / C::kStages) & 1);
-          for (int t = 0; t < n_qt && ready && j > 0; ++t) ready = mbar_test_wait(&s_free[t], (j - 1) & 1);
-          if (ready) {
+        for (int t = 0; t < n_qt; ++t) {
+          const int j = pv_next[t];
+          if (j < s_next[t] && mbar_test_wait(&p_full[t], j & 1) &&
+              mbar_test_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1)) {
             tc::fence_after();
-            const uint32_t kaddr = sbase + C::kOffKV + st * 2 * C::kKVTile;
-            for (int t = 0; t < n_qt; ++t) {
-              const uint32_t d_s = tmem + C::kColS + t * C::kKeys;
-              const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
+            const uint32_t vaddr = sbase + C::kOffV + (j % C::kVStages) * C::kKVTile;
+            const uint32_t p_tmem = tmem + t * C::kKeys;  // 16 keys = 8 columns per k-step
+            const uint32_t d_o = tmem + C::kColO + t * D;
 #pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off_q = (ks >> 2) * 16384 + (ks & 3) * 32;
-                const uint32_t off_k = (ks >> 2) * (C::kKeys * 128) + (ks & 3) * 32;
-                tc::mma_bf16(d_s, tc::sw128_desc(qaddr + off_q, 16, 1024),
-                             tc::sw128_desc(kaddr + off_k, 16, 1024), id_s, ks > 0);
-              }
-              tc::commit(&s_full[t]);
-            }
-            ++s_next;
+            for (int ks = 0; ks < C::kKeys / 16; ++ks)
+              tc::mma_bf16_ts(d_o, p_tmem + ks * 8, tc::sw128_desc(vaddr + ks * 2048, C::kPanelBytes, 1024), id_o,
+                              j > 0 || ks > 0);
+            tc::commit(&o_done[t]);
+            pv_next[t] = j + 1;
+            if (pv_next[1 - t] > j) tc::commit(&v_empty[j % C::kVStages]);
             progressed = true;
           }
         }
         for (int t = 0; t < n_qt; ++t) {
-          const int j = pv_next[t];
-          if (j >= s_next) continue;  // S(j) not issued yet (nor P(j) written)
-          const int b = j & 1;
-          if (!mbar_test_wait(&p_full[2 * t + b], (j >> 1) & 1)) continue;
-          tc::fence_after();
-          const int st = j % C::kStages;
-          const uint32_t vaddr = sbase + C::kOffKV + st * 2 * C::kKVTile + C::kKVTile;
-          const uint32_t p_tmem = tmem + C::kColP + t * 64 + b * 32;  // 16 keys = 8 columns per k-step
-          const uint32_t d_o = tmem + C::kColO + t * D;
+          const int j = s_next[t];
+          if (j < nkv && pv_next[t] == j && mbar_test_wait(&k_full[j % C::kKStages], (j / C::kKStages) & 1) &&
+              (j == 0 || mbar_test_wait(&o_done[t], (j - 1) & 1))) {
+            tc::fence_after();
+            const uint32_t kaddr = sbase + C::kOffK + (j % C::kKStages) * C::kKVTile;
+            const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
+            const uint32_t d_s = tmem + t * C::kKeys;
 #pragma unroll
-          for (int ks = 0; ks < C::kKeys / 16; ++ks)
-            tc::mma_bf16_ts(d_o, p_tmem + ks * 8, tc::sw128_desc(vaddr + ks * 2048, C::kKeys * 128, 1024), id_o,
-                            j > 0 || ks > 0);
-          tc::commit(&o_done[2 * t + b]);
-          pv_next[t] = j + 1;
-          progressed = true;
-          // the stage is free once both tiles' PV(j) are issued (commit
-          // arrives after every MMA issued so far has completed)
-          const int other = n_qt > 1 ? pv_next[1 - t] : nkv;
-          if (other > j) tc::commit(&kv_empty[st]);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off_q = (ks >> 2) * 16384 + (ks & 3) * 32;
+              const uint32_t off_k = (ks >> 2) * C::kPanelBytes + (ks & 3) * 32;
+              tc::mma_bf16(d_s, tc::sw128_desc(qaddr + off_q, 16, 1024), tc::sw128_desc(kaddr + off_k, 16, 1024),
+                           id_s, ks > 0);
+            }
+            tc::commit(&s_full[t]);
+            s_next[t] = j + 1;
+            if (s_next[1 - t] > j) tc::commit(&k_empty[j % C::kKStages]);
+            progressed = true;
+          }
         }
         idle = progressed ? 0 : idle + 1;
       }
@@ -226,7 +285,8 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     const int t = warp >> 2;
     const int r = ((warp & 3) << 5) + lane;
     const int m = t * 128 + r;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t row_s = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16) + t * C::kKeys;
+    const uint32_t row_o = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16) + C::kColO + t * D;
     int row = -1, pos = -1, qh = 0;
     if (m < M) {
       row = p.row_list[it.rows_off + m / G];
@@ -237,39 +297,34 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
-      const int b = j & 1;
       ok = warp_wait(&s_full[t], j & 1, err);
       if (!ok) break;
       tc::fence_after();
-      uint32_t sr[64];
-      tc::ld32(tmem + lane_base + C::kColS + t * C::kKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tc::ld32(tmem + lane_base + C::kColS + t * C::kKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[t]);
-
       // columns <= lim are visible: causal, and inside the item's key run
       // (the tile past the run's end holds stand-in pages)
       const int lim = min(pos - (it.key_base + C::kKeys * j), it.n_keys - 1 - C::kKeys * j);
-      float f[64];
+      const bool masked = !__all_sync(0xffffffffu, lim >= C::kKeys - 1);
+      // The whole S row in registers (4 loads of 32 columns in flight at
+      // once), its max (scale > 0 commutes with max), then the weights per
+      // chunk of 32 columns; P (bf16 pairs) of chunk c goes to columns
+      // 16c..16c+15, which hold scores already in registers.
+      uint32_t sr[C::kKeys];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) f[c] = __uint_as_float(sr[c]);
-      if (!__all_sync(0xffffffffu, lim >= 63)) {
+      for (int c = 0; c < C::kKeys / 32; ++c) tc::ld32(row_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      tc::wait_ld();
+      if (masked) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) f[c] = c <= lim ? f[c] : -INFINITY;
+        for (int e = 0; e < C::kKeys; ++e)
+          if (e > lim) sr[e] = __float_as_uint(-INFINITY);
       }
-      // row max with 8 independent chains (scale > 0, so the max commutes with it)
-      float m8[8];
+      float m4[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = f[i];
+      for (int i = 0; i < 4; ++i) m4[i] = -INFINITY;
 #pragma unroll
-      for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], f[c]);
-#pragma unroll
-      for (int w2 = 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-        for (int i = 0; i < w2; ++i) m8[i] = fmaxf(m8[i], m8[i + w2]);
-      const float mx = m8[0] * qk_scale;
+      for (int e = 0; e < C::kKeys / 2; ++e)
+        m4[e & 3] = max3(m4[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+      m4[0] = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      const float mx = m4[0] * qk_scale;
       float alpha = 1.f;
       bool resc = false;
       const float m_new = fmaxf(m_run, mx);
@@ -279,63 +334,43 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         resc = true;
       }
       const float nb = m_run == -INFINITY ? 0.f : -m_run;
-      float s8[8];
+      uint64_t acc[4] = {0, 0, 0, 0};  // packed pairs of partial row sums
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s8[i] = 0.f;
-      uint32_t pk[32];
+      for (int c = 0; c < C::kKeys / 32; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float e0 = ex2(fmaf(f[2 * c], qk_scale, nb)), e1 = ex2(fmaf(f[2 * c + 1], qk_scale, nb));
-        s8[(2 * c) & 7] += e0;
-        s8[(2 * c + 1) & 7] += e1;
-        pk[c] = pack_bf16(e0, e1);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = softmax_pair(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1]), qk_scale,
+                               nb, acc[e & 3]);
+        tc::st16(row_s + 16 * c, pk);
       }
+      const float row_sum = (sum_pair(acc[0]) + sum_pair(acc[1])) + (sum_pair(acc[2]) + sum_pair(acc[3]));
+      l_run = l_run * alpha + row_sum;
+      // O rescale: PV_t(j-1) is complete (S_t(j) was issued after it)
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
-      for (int w2 = 4; w2 >= 1; w2 >>= 1)
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tc::ld32(row_o + cc * 32, o);
+          tc::wait_ld();
 #pragma unroll
-        for (int i = 0; i < w2; ++i) s8[i] += s8[i + w2];
-      const float sum = s8[0];
-      l_run = l_run * alpha + sum;
-      // P buffer b is free once PV(j-2) is done; a rescale of O needs every
-      // PV so far (up to j-1) done -- commits complete in issue order.
-      const bool any_resc = j > 0 && __any_sync(0xffffffffu, resc);
-      if (any_resc) {
-        ok = warp_wait(&o_done[2 * t + ((j - 1) & 1)], ((j - 1) >> 1) & 1, err);
-      } else if (j >= 2) {
-        ok = warp_wait(&o_done[2 * t + b], ((j - 2) >> 1) & 1, err);
-      }
-      if (!ok) break;
-      tc::fence_after();
-      if (any_resc) {
-        {
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            const uint32_t ta = tmem + lane_base + C::kColO + t * D + cc * 32;
-            tc::ld32(ta, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::st32(ta, o);
-          }
-          tc::wait_st();
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::st32(row_o + cc * 32, o);
         }
       }
-      // P as bf16 pairs (key 2c in the low half of column c): the A operand of PV(j)
-      tc::st32(tmem + lane_base + C::kColP + t * 64 + b * 32, pk);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[2 * t + b]);
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    if (ok) ok = warp_wait(&o_done[2 * t + ((nkv - 1) & 1)], ((nkv - 1) >> 1) & 1, err);
+    if (ok) ok = warp_wait(&o_done[t], (nkv - 1) & 1, err);
     tc::fence_after();
     if (ok) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        tc::ld32(tmem + lane_base + C::kColO + t * D + cc * 32, o);
+        tc::ld32(row_o + cc * 32, o);
         tc::wait_ld();
         if (row < 0) continue;
         if (it.part < 0) {
