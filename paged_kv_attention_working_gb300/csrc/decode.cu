@@ -48,7 +48,7 @@ struct DecodeCfg {
 };
 
 template <bool E4M3, int D>
-__global__ void __launch_bounds__(kThreads) decode_kernel(Geometry g, PlanView p, int layer,
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanView p, int layer,
                                                           const __nv_bfloat16* __restrict__ q,
                                                           const uint8_t* __restrict__ kpool,
                                                           const uint8_t* __restrict__ vpool,
