@@ -35,6 +35,31 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
+def kernel_sources_sha(files):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_attention_working_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic(key, files, algorithmic):
+    """DRAM bytes per launch (read + write) of a kernel from the ncu capture
+    recorded in profiles/traffic.json, scaled by algorithmic work when the
+    capture ran a smaller case of the same workload; None when the kernel's
+    sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(key)
+    if not rec or rec.get("source_sha256") != kernel_sources_sha(files):
+        return None
+    return rec["dram_bytes_per_launch"] * algorithmic / rec["algorithmic_per_launch"]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -364,7 +389,8 @@ def run_gpu(args, w, world, rank, local):
         "rows_per_s": world * n_rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
                      "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak,
+                     "traffic": traffic(f"decode_kernel {w.name}", ["decode.cu", "ptx.cuh", "plan.h"], attend_bytes),
                      "algorithmic_bytes_per_launch": attend_bytes, "avg_launch_ms": attend_avg},
         "append": {"bytes_per_launch": append_bytes},
         "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
@@ -463,7 +489,9 @@ def run_mixed(args, w, world, rank, local):
                       "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1},
            "roofline": {"bound": "tensor", "kernel": "prefill_kernel (chunks-only attend)", "achieved": tflops,
                         "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": tflops / peak,
-                        "traffic": None, "flops_per_launch": flops, "avg_launch_ms": t_chunks},
+                        "traffic": traffic(f"prefill_kernel {w.name}", ["prefill.cu", "ptx.cuh", "tcgen05.cuh", "plan.h"],
+                                           flops),
+                        "flops_per_launch": flops, "avg_launch_ms": t_chunks},
            "mixed_step": {"attend_ms": t_mixed, "rows": sum(s[1] for s in main_segs),
                           "rows_per_s": sum(s[1] for s in main_segs) / (t_mixed * 1e-3),
                           "decode_kv_bytes": dec_keys * Hkv * D * 2 * 2}}

@@ -242,6 +242,10 @@ pie_status pie_batch_items(const pie_batch* b, int32_t kind, int32_t* out, int32
  * bit 0 = a bounded wait inside a kernel ran out (that launch's results are
  * invalid).  0 = no error. */
 pie_status pie_ctx_check(pie_ctx* ctx, int32_t* flags);
+/* Error-path self-test: enqueues one kernel whose mbarrier wait can never
+ * complete, bounded at `polls` polls; it records bit 0 in the error word
+ * (read it with pie_ctx_check) and ends.  The context stays usable. */
+pie_status pie_selftest_wait_timeout(pie_ctx* ctx, int32_t polls);
 
 #ifdef __cplusplus
 }

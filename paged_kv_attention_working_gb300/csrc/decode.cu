@@ -426,6 +426,22 @@ cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const
   return cudaErrorInvalidValue;
 }
 
+namespace {
+// One thread waits on an mbarrier that nothing ever completes; the bounded
+// wait gives up after `polls` polls and records the timeout bit.
+__global__ void wait_selftest_kernel(int* err, uint32_t polls) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0, err, polls);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* err, uint32_t polls, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 1, 0, st>>>(err, polls);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float* lse, const float* part_acc,
                          const float* part_ml, cudaStream_t st) {
   if (p.n_merge == 0) return cudaSuccess;

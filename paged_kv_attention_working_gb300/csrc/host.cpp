@@ -797,6 +797,14 @@ pie_status pie_ctx_check(pie_ctx* c, int32_t* flags) {
   return PIE_OK;
 }
 
+pie_status pie_selftest_wait_timeout(pie_ctx* c, int32_t polls) {
+  if (!c || polls <= 0) return PIE_ERR_INVALID;
+  if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
+  cudaError_t e = pie::launch_wait_selftest(c->d_err, static_cast<uint32_t>(polls), c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "self-test launch");
+  return PIE_OK;
+}
+
 pie_status pie_batch_plan_info(const pie_batch* b, int32_t* info) {
   if (!b || !info) return PIE_ERR_INVALID;
   info[0] = b->view.n_dec;

@@ -29,7 +29,7 @@ EXPORTS = [
     "pie_ws_fork", "pie_ws_freeze", "pie_ws_rollback", "pie_ws_match_prefix", "pie_ws_info",
     "pie_ws_page_table", "pie_page_refcount", "pie_free_pages", "pie_batch_begin", "pie_batch_rows",
     "pie_batch_slots", "pie_kv_append", "pie_attend", "pie_batch_end", "pie_batch_plan_info",
-    "pie_batch_items", "pie_ctx_check", "pie_attend_decode_noalloc",
+    "pie_batch_items", "pie_ctx_check", "pie_attend_decode_noalloc", "pie_selftest_wait_timeout",
 ]
 PIE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -94,6 +94,7 @@ def _load():
         "pie_batch_items": [V, I, P(I), I, P(I)],
         "pie_ctx_check": [V, P(I)],
         "pie_attend_decode_noalloc": [P(pie_decode_args)],
+        "pie_selftest_wait_timeout": [V, I],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -169,6 +170,10 @@ def pie_ctx_check(ctx) -> int:
     v = ctypes.c_int32()
     _check(ctx, lib.pie_ctx_check(ctx, ctypes.byref(v)), "pie_ctx_check")
     return v.value
+
+
+def pie_selftest_wait_timeout(ctx, polls) -> None:
+    _check(ctx, lib.pie_selftest_wait_timeout(ctx, polls), "pie_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------- working sets

@@ -111,3 +111,17 @@ def test_empty_batch_is_a_no_op():
     pie.pie_batch_end(g.ctx, b)
     assert pie.pie_ctx_check(g.ctx) == 0
     g.close()
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """A kernel wait that can never complete ends after its poll limit, sets
+    the error bit the host reads, and leaves the context usable."""
+    w = wl.tiny_decode()
+    g = gpu_driver.GpuRun(w)
+    assert pie.pie_ctx_check(g.ctx) == 0
+    pie.pie_selftest_wait_timeout(g.ctx, 1000)
+    assert pie.pie_ctx_check(g.ctx) == 1
+    assert pie.pie_ctx_check(g.ctx) == 0          # read and cleared
+    passes = g.run()                               # the full workload still runs and checks clean
+    assert passes and pie.pie_ctx_check(g.ctx) == 0
+    g.close()
