@@ -390,7 +390,7 @@ def run_gpu(args, w, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
                      "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / hbm_peak,
-                     "traffic": traffic(f"decode_kernel {w.name}", ["decode.cu", "ptx.cuh", "plan.h"], attend_bytes),
+                     "traffic": traffic(f"decode_kernel {w.name}", ["decode.cu", "ptx.cuh"], attend_bytes),
                      "algorithmic_bytes_per_launch": attend_bytes, "avg_launch_ms": attend_avg},
         "append": {"bytes_per_launch": append_bytes},
         "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
@@ -489,7 +489,7 @@ def run_mixed(args, w, world, rank, local):
                       "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1},
            "roofline": {"bound": "tensor", "kernel": "prefill_kernel (chunks-only attend)", "achieved": tflops,
                         "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": tflops / peak,
-                        "traffic": traffic(f"prefill_kernel {w.name}", ["prefill.cu", "ptx.cuh", "tcgen05.cuh", "plan.h"],
+                        "traffic": traffic(f"prefill_kernel {w.name}", ["prefill.cu", "ptx.cuh", "tcgen05.cuh"],
                                            flops),
                         "flops_per_launch": flops, "avg_launch_ms": t_chunks},
            "mixed_step": {"attend_ms": t_mixed, "rows": sum(s[1] for s in main_segs),
