@@ -414,11 +414,14 @@ def run_mixed(args, w, world, rank, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
-    block = 16 * D * 2
+    esize = 2 if w.kv_dtype == 0 else 1
+    block = 16 * D * esize
     pool_bytes = w.num_layers * w.num_pages * Hkv * block
     kpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
     vpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
-    ctx = pie.pie_ctx_create(w.num_layers, Hq, Hkv, D, w.num_pages, free_list=w.free_list().tolist(),
+    ks, vs = w.scales()
+    ctx = pie.pie_ctx_create(w.num_layers, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype,
+                             free_list=w.free_list().tolist(), k_scale=ks, v_scale=vs,
                              k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000 + rank)
@@ -483,9 +486,11 @@ def run_mixed(args, w, world, rank, local):
             peak, src = float(d["bf16_tflops"]), "measured"
     res = {"metric": "prefill attend TFLOP/s (causal-exact flops)", "value": tflops, "unit": "TFLOP/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mixed,
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16" if w.kv_dtype == 0 else "e4m3 KV as f16 operands, f16 Q/P, fp32 accumulate",
            "data": "synthetic",
-           "config": {"workload": w.name, "chunks": len(chunk_segs), "chunk_rows": sum(s[1] for s in chunk_segs),
+           "config": {"workload": w.name, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
+                      "chunks": len(chunk_segs), "chunk_rows": sum(s[1] for s in chunk_segs),
                       "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1},
            "roofline": {"bound": "tensor", "kernel": "prefill_kernel (chunks-only attend)", "achieved": tflops,
                         "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": tflops / peak,
@@ -494,7 +499,7 @@ def run_mixed(args, w, world, rank, local):
                         "flops_per_launch": flops, "avg_launch_ms": t_chunks},
            "mixed_step": {"attend_ms": t_mixed, "rows": sum(s[1] for s in main_segs),
                           "rows_per_s": sum(s[1] for s in main_segs) / (t_mixed * 1e-3),
-                          "decode_kv_bytes": dec_keys * Hkv * D * 2 * 2}}
+                          "decode_kv_bytes": dec_keys * Hkv * D * esize * 2}}
     pie.pie_ctx_destroy(ctx)
     return res
 
@@ -509,7 +514,7 @@ def main():
                     help="CPU seconds of oracle work (whole reference run, or the cpu_baseline sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "mixed_batch", "llama70b_fp8"])
+                    choices=["llama8b_decode", "mixed_batch", "mixed_batch_e4m3", "llama70b_fp8"])
     ap.add_argument("--n-ws", type=int, default=0,
                     help="working sets of the e4m3 workload (0 = the full 256; fewer only for profiling)")
     ap.add_argument("--layers", type=int, default=32,
@@ -518,8 +523,14 @@ def main():
     from paged_kv_attention_working_gb300 import workloads as wl
 
     world, rank, local = dist_init()
-    if args.workload == "mixed_batch":
-        res = run_mixed(args, wl.mixed_batch(), world, rank, local)
+    if args.workload.startswith("mixed_batch"):
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the decode workloads; "
+                                  "the mixed batch is timed on the GPU only"}), flush=True)
+            return
+        kv = wl.KV_E4M3 if args.workload.endswith("e4m3") else wl.KV_BF16
+        res = run_mixed(args, wl.mixed_batch(name=args.workload, kv_dtype=kv), world, rank, local)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

@@ -169,7 +169,12 @@ pie_status pie_kv_append(pie_ctx* ctx, pie_batch* b, int32_t layer,
  * log of the softmax denominator) or NULL.  Row r at position p of working
  * set w, query head h: softmax over keys 0..p of w, from KV head h / (Hq /
  * Hkv), of (q . k) / sqrt(d), applied to the values.  Requires that
- * pie_kv_append ran for this layer and batch first. */
+ * pie_kv_append ran for this layer and batch first.
+ * Precision: keys and values enter as stored (bf16, or the e4m3 code times
+ * its scale); scores and sums are fp32; the softmax weights meet V as bf16
+ * (bf16 pools) or f16 (e4m3 pools).  With an e4m3 pool, rows that take the
+ * tensor-core path (prefill chunks, large fork groups) also round q to f16,
+ * so |q| must stay below 65504 there. */
 pie_status pie_attend(pie_ctx* ctx, pie_batch* b, int32_t layer,
                       const void* q, void* out, float* lse);
 /* Closes the batch.  Its device work stays enqueued on the stream. */

@@ -776,8 +776,8 @@ pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, vo
   float* ml = c->d_part + total_parts * c->geo.hq * c->geo.d;
   cudaError_t e = cudaSuccess;
   if (v.n_pre)
-    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, out, lse, acc, ml, c->d_err,
-                            c->stream);
+    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
+                            lse, acc, ml, c->d_err, c->stream);
   if (e == cudaSuccess && v.n_dec)
     e = pie::launch_decode(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
                            lse, acc, ml, c->d_err, c->stream);

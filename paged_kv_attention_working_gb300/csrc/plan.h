@@ -61,8 +61,9 @@ cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const
                           const float* scale_v, void* out, float* lse, float* part_acc,
                           float* part_ml, int* err, cudaStream_t st);
 cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, const void* q,
-                           const void* kpool, const void* vpool, void* out, float* lse,
-                           float* part_acc, float* part_ml, int* err, cudaStream_t st);
+                           const void* kpool, const void* vpool, const float* scale_k,
+                           const float* scale_v, void* out, float* lse, float* part_acc,
+                           float* part_ml, int* err, cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint32_t polls, cudaStream_t st);
 cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float* lse,
                          const float* part_acc, const float* part_ml, cudaStream_t st);

@@ -28,6 +28,15 @@
 // Tensor memory: S/P of tile t at columns t*128, O of tile t at 256 + t*d.
 // Rows with one part are normalised and written as bf16; otherwise the
 // fp32 (acc, m, l) partial goes to the merge kernel.
+//
+// e4m3 pools (d = 128): the tensor cores take the dequantised codes.  The
+// producer copies raw e4m3 page blocks into a small staging ring; two
+// converter warps turn each 16-key page into f16 (every e4m3 value is exact
+// in f16) at its place in the 128-byte-swizzled K / V tile, and hand the
+// tile to the MMA thread.  Q is rounded to f16 on load and P is written as
+// f16 pairs, so both products are f16 x f16 with fp32 accumulation; the
+// per-(layer, KV head) scales fold into the softmax scale (K) and the
+// output (V), as in the decode kernel.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -39,23 +48,28 @@
 namespace pie {
 namespace {
 
-constexpr int kThreadsPre = 320;  // 8 softmax warps, MMA warp 8, producer warp 9
-
-template <int D>
+// Warps 0-7 softmax, warp 8 MMA, warp 9 producer; e4m3 adds converter
+// warps 10 and 11.
+template <int D, bool E4M3>
 struct PreCfg {
+  static constexpr int kThreads = E4M3 ? 384 : 320;
   static constexpr int kPanels = D / 64;
   static constexpr int kKeys = 128;                       // keys per tile
   static constexpr int kPagesPerTile = kKeys / kPageSize;  // 8
   static constexpr int kQTile = 128 * D * 2;
-  static constexpr int kKVTile = kKeys * D * 2;            // one K (or V) tile
+  static constexpr int kKVTile = kKeys * D * 2;            // one K (or V) tile, 16-bit elements
   static constexpr int kPanelBytes = kKeys * 128;          // one 64-column panel of a tile
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 3;
+  static constexpr int kKStages = E4M3 ? 2 : (D == 128 ? 3 : 4);
+  static constexpr int kVStages = E4M3 ? 2 : (D == 128 ? 2 : 3);
+  static constexpr int kRawRing = 2;                       // e4m3 staging: K(j), V(j) alternate
+  static constexpr int kRawStages = E4M3 ? kRawRing : 0;
+  static constexpr int kRawTile = kKeys * D;               // one e4m3 tile (8 page blocks)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQTile;
   static constexpr int kOffV = kOffK + kKStages * kKVTile;
-  static constexpr int kOffBar = kOffV + kVStages * kKVTile;
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
+  static constexpr int kOffRaw = kOffV + kVStages * kKVTile;
+  static constexpr int kOffBar = kOffRaw + kRawStages * kRawTile;
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 * kRawStages;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
@@ -69,26 +83,55 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // Two softmax weights: e = 2^(s * scale + nb) for a pair of scores (one
 // packed f32x2 FMA, two ex2), added to a packed pair of running sums;
-// returns the pair as bf16x2 (element 0 low).
+// returns the pair as bf16x2, or f16x2 when F16 (element 0 low).
+template <bool F16>
 __device__ __forceinline__ uint32_t softmax_pair(float s0, float s1, float scale, float nb, uint64_t& acc) {
   uint32_t pk;
-  asm("{\n"
-      " .reg .b64 s, k, n, x, e;\n"
-      " .reg .f32 x0, x1, e0, e1;\n"
-      " mov.b64 s, {%2, %3};\n"
-      " mov.b64 k, {%4, %4};\n"
-      " mov.b64 n, {%5, %5};\n"
-      " fma.rn.f32x2 x, s, k, n;\n"
-      " mov.b64 {x0, x1}, x;\n"
-      " ex2.approx.ftz.f32 e0, x0;\n"
-      " ex2.approx.ftz.f32 e1, x1;\n"
-      " mov.b64 e, {e0, e1};\n"
-      " add.rn.f32x2 %1, %1, e;\n"
-      " cvt.rn.bf16x2.f32 %0, e1, e0;\n"
-      "}"
-      : "=r"(pk), "+l"(acc)
-      : "f"(s0), "f"(s1), "f"(scale), "f"(nb));
+  if constexpr (F16) {
+    asm("{\n"
+        " .reg .b64 s, k, n, x, e;\n"
+        " .reg .f32 x0, x1, e0, e1;\n"
+        " mov.b64 s, {%2, %3};\n"
+        " mov.b64 k, {%4, %4};\n"
+        " mov.b64 n, {%5, %5};\n"
+        " fma.rn.f32x2 x, s, k, n;\n"
+        " mov.b64 {x0, x1}, x;\n"
+        " ex2.approx.ftz.f32 e0, x0;\n"
+        " ex2.approx.ftz.f32 e1, x1;\n"
+        " mov.b64 e, {e0, e1};\n"
+        " add.rn.f32x2 %1, %1, e;\n"
+        " cvt.rn.f16x2.f32 %0, e1, e0;\n"
+        "}"
+        : "=r"(pk), "+l"(acc)
+        : "f"(s0), "f"(s1), "f"(scale), "f"(nb));
+  } else {
+    asm("{\n"
+        " .reg .b64 s, k, n, x, e;\n"
+        " .reg .f32 x0, x1, e0, e1;\n"
+        " mov.b64 s, {%2, %3};\n"
+        " mov.b64 k, {%4, %4};\n"
+        " mov.b64 n, {%5, %5};\n"
+        " fma.rn.f32x2 x, s, k, n;\n"
+        " mov.b64 {x0, x1}, x;\n"
+        " ex2.approx.ftz.f32 e0, x0;\n"
+        " ex2.approx.ftz.f32 e1, x1;\n"
+        " mov.b64 e, {e0, e1};\n"
+        " add.rn.f32x2 %1, %1, e;\n"
+        " cvt.rn.bf16x2.f32 %0, e1, e0;\n"
+        "}"
+        : "=r"(pk), "+l"(acc)
+        : "f"(s0), "f"(s1), "f"(scale), "f"(nb));
+  }
   return pk;
+}
+
+// Eight bf16 (one 16-byte chunk) -> eight f16, round to nearest even.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  auto cv = [](uint32_t w) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    return pack_f16(lo, hi);
+  };
+  return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
 }
 
 __device__ __forceinline__ float sum_pair(uint64_t acc) {
@@ -102,13 +145,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreadsPre, 1)
+template <int D, bool E4M3>
+__global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     prefill_kernel(Geometry g, PlanView p, int layer, const __nv_bfloat16* __restrict__ q,
                    const uint8_t* __restrict__ kpool, const uint8_t* __restrict__ vpool,
+                   const float* __restrict__ kscale, const float* __restrict__ vscale,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_acc,
                    float* __restrict__ part_ml, int* err) {
-  using C = PreCfg<D>;
+  using C = PreCfg<D, E4M3>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -121,6 +165,8 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   uint64_t* s_full = v_empty + C::kVStages;       // [tile]: S_t(j) in tensor memory
   uint64_t* p_full = s_full + 2;                  // [tile]: P_t(j) written (and O rescaled)
   uint64_t* o_done = p_full + 2;                  // [tile]: PV_t(j) complete
+  uint64_t* raw_full = o_done + 2;                // [raw stage] (e4m3 only)
+  uint64_t* raw_empty = raw_full + C::kRawStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const WorkItem it = p.pre_items[blockIdx.x];
@@ -132,13 +178,18 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // e4m3: a K / V stage is filled by the two converter warps' arrivals
     for (int s = 0; s < C::kKStages; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], E4M3 ? 2 : 1);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < C::kVStages; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], E4M3 ? 2 : 1);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < C::kRawStages; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -151,7 +202,7 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   {
     constexpr int kChunks = D / 8;  // 16-byte chunks per row
     const int total = n_qt * 128 * kChunks;
-    for (int idx = threadIdx.x; idx < total; idx += kThreadsPre) {
+    for (int idx = threadIdx.x; idx < total; idx += C::kThreads) {
       int m = idx / kChunks, c16 = idx % kChunks;
       int t = m >> 7, r = m & 127;
       uint4 v = make_uint4(0, 0, 0, 0);
@@ -159,6 +210,7 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         int row = p.row_list[it.rows_off + m / G];
         int qh = head * G + m % G;
         v = *reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(row) * g.hq + qh) * D + c16 * 8);
+        if constexpr (E4M3) v = bf16x8_to_f16x8(v);
       }
       int panel = c16 >> 3, c = c16 & 7;
       *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
@@ -174,7 +226,80 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
+  if (E4M3 && warp == 9) {
+    // ------------------------------------------------- producer (e4m3)
+    // Raw tiles in order K(0), V(0), K(1), V(1), ...: one 2-KB page block
+    // per lane 0..7 into the staging ring.
+    const int64_t layer_blk = static_cast<int64_t>(layer) * g.num_pages * g.hkv;
+    bool ok = true;
+    for (int i = 0; i < 2 * nkv && ok; ++i) {
+      const int r = i % C::kRawRing, j = i >> 1;
+      if (i >= C::kRawRing) ok = warp_wait(&raw_empty[r], ((i / C::kRawRing) - 1) & 1, err);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&raw_full[r], C::kRawTile);
+      __syncwarp();
+      if (lane < C::kPagesPerTile) {
+        int pj = C::kPagesPerTile * j + lane;
+        if (pj >= it.n_pages) pj = it.n_pages - 1;  // keys there are masked; any finite page will do
+        const int page = p.page_ids[it.pages_off + pj];
+        const int64_t off = (layer_blk + static_cast<int64_t>(page) * g.hkv + head) * g.block_bytes;
+        bulk_g2s(smem + C::kOffRaw + r * C::kRawTile + lane * 2048, ((i & 1) ? vpool : kpool) + off, 2048,
+                 &raw_full[r]);
+      }
+      __syncwarp();
+    }
+  } else if (E4M3 && warp >= 10) {
+    // ------------------------------------------------ converters (e4m3)
+    // Raw page block pg holds key s's 16-byte chunk c (dims 16c..16c+15) at
+    // s*128 + 16*(c ^ (s%8)); the 8 blocks of a tile are contiguous, so raw
+    // chunk qc belongs to tile key qc/8.  Its f16 values go to dims
+    // 16c..16c+15 of that key's tile row: panel c/4, 16-byte f16 chunks
+    // 2(c%4) and 2(c%4)+1, each at key*128 + 16*(chunk ^ (key%8)).
+    // Thread ct takes raw chunks ct + 64n (n = 0..15): keys ct/8 + 8n, all
+    // with key%8 = ct/8 and the same physical chunk ct%8, so every address
+    // offset but the 1-KB row step is fixed per thread.  Threads with c >= 4
+    // store their second chunk first, so the 8 lanes of a store phase hit 8
+    // distinct bank groups.
+    const int ct = threadIdx.x - 320;
+    const int kr = ct >> 3, c = (ct & 7) ^ kr, ca = 2 * (c & 3);
+    const int off_lo = (c >> 2) * C::kPanelBytes + kr * 128 + ((ca ^ kr) << 4);
+    const int off_hi = (c >> 2) * C::kPanelBytes + kr * 128 + (((ca + 1) ^ kr) << 4);
+    const int off_1 = (c & 4) ? off_hi : off_lo, off_2 = (c & 4) ? off_lo : off_hi;
+    bool ok = true;
+    for (int i = 0; i < 2 * nkv && ok; ++i) {
+      const int r = i % C::kRawRing, j = i >> 1;
+      const bool is_v = i & 1;
+      const int nst = is_v ? C::kVStages : C::kKStages;
+      const int st = j % nst;
+      ok = warp_wait(&raw_full[r], (i / C::kRawRing) & 1, err);
+      if (ok && j >= nst) ok = warp_wait(is_v ? &v_empty[st] : &k_empty[st], ((j / nst) - 1) & 1, err);
+      if (!ok) break;
+      const uint8_t* src = smem + C::kOffRaw + r * C::kRawTile + ct * 16;
+      uint8_t* dst = smem + (is_v ? C::kOffV : C::kOffK) + st * C::kKVTile;
+#pragma unroll 1
+      for (int n0 = 0; n0 < C::kKeys / 8; n0 += 4) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const uint4*>(src + (n0 + u) * 1024);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 a = make_uint4(e4m3x2_lo_to_f16x2(w[u].x), e4m3x2_hi_to_f16x2(w[u].x),
+                                     e4m3x2_lo_to_f16x2(w[u].y), e4m3x2_hi_to_f16x2(w[u].y));
+          const uint4 b = make_uint4(e4m3x2_lo_to_f16x2(w[u].z), e4m3x2_hi_to_f16x2(w[u].z),
+                                     e4m3x2_lo_to_f16x2(w[u].w), e4m3x2_hi_to_f16x2(w[u].w));
+          uint8_t* rowp = dst + (n0 + u) * 1024;
+          *reinterpret_cast<uint4*>(rowp + off_1) = (c & 4) ? b : a;
+          *reinterpret_cast<uint4*>(rowp + off_2) = (c & 4) ? a : b;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&raw_empty[r]);
+        mbar_arrive(is_v ? &v_full[st] : &k_full[st]);
+      }
+    }
+  } else if (warp == 9) {
     // ------------------------------------------------------------ producer
     // K(j) and V(j) each take one copy per lane: 8 pages x kPanels panels.
     const int64_t layer_blk = static_cast<int64_t>(layer) * g.num_pages * g.hkv;
@@ -229,8 +354,8 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     // overwrites P_t(j-1)).  A K (V) stage is released by a commit after the
     // last S (PV) that reads it.
     if (lane == 0) {
-      const uint32_t id_s = tc::idesc_bf16(128, C::kKeys, false, false);
-      const uint32_t id_o = tc::idesc_bf16(128, D, false, true);
+      const uint32_t id_s = tc::idesc_f16kind(128, C::kKeys, false, false, !E4M3);
+      const uint32_t id_o = tc::idesc_f16kind(128, D, false, true, !E4M3);
       int s_next[2] = {0, n_qt > 1 ? 0 : nkv};
       int pv_next[2] = {0, n_qt > 1 ? 0 : nkv};
       uint32_t idle = 0;
@@ -293,7 +418,8 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
       pos = p.row_pos[row];
       qh = head * G + m % G;
     }
-    const float qk_scale = 1.4426950408889634f * rsqrtf(static_cast<float>(D));
+    const float qk_scale = (E4M3 ? kscale[layer * g.hkv + head] : 1.0f) * 1.4426950408889634f *
+                           rsqrtf(static_cast<float>(D));
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
@@ -340,7 +466,7 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = softmax_pair(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1]), qk_scale,
+          pk[e] = softmax_pair<E4M3>(__uint_as_float(sr[32 * c + 2 * e]), __uint_as_float(sr[32 * c + 2 * e + 1]), qk_scale,
                                nb, acc[e & 3]);
         tc::st16(row_s + 16 * c, pk);
       }
@@ -366,7 +492,8 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
     if (ok) ok = warp_wait(&o_done[t], (nkv - 1) & 1, err);
     tc::fence_after();
     if (ok) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float vdq = E4M3 ? vscale[layer * g.hkv + head] : 1.0f;
+      const float inv = l_run > 0.f ? vdq / l_run : 0.f;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -389,8 +516,8 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
           float4* dst = reinterpret_cast<float4*>(part_acc + slot * D + cc * 32);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                 __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * vdq, __uint_as_float(o[4 * v + 1]) * vdq,
+                                 __uint_as_float(o[4 * v + 2]) * vdq, __uint_as_float(o[4 * v + 3]) * vdq);
         }
       }
       if (row >= 0) {
@@ -411,32 +538,40 @@ __global__ void __launch_bounds__(kThreadsPre, 1)
   }
 }
 
-template <int D>
+template <int D, bool E4M3>
 cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
-                     const void* vpool, void* out, float* lse, float* acc, float* ml, int* err, cudaStream_t st) {
-  using C = PreCfg<D>;
+                     const void* vpool, const float* kscale, const float* vscale, void* out, float* lse, float* acc,
+                     float* ml, int* err, cudaStream_t st) {
+  using C = PreCfg<D, E4M3>;
+  static_assert(C::kSmem <= 227 * 1024, "shared memory budget");
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<D, E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   dim3 grid(p.n_pre, g.hkv);
-  prefill_kernel<D><<<grid, kThreadsPre, C::kSmem, st>>>(
+  prefill_kernel<D, E4M3><<<grid, C::kThreads, C::kSmem, st>>>(
       g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
-      static_cast<const uint8_t*>(vpool), static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
+      static_cast<const uint8_t*>(vpool), kscale, vscale, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
-                           const void* vpool, void* out, float* lse, float* part_acc, float* part_ml, int* err,
-                           cudaStream_t st) {
+                           const void* vpool, const float* scale_k, const float* scale_v, void* out, float* lse,
+                           float* part_acc, float* part_ml, int* err, cudaStream_t st) {
   if (p.n_pre == 0) return cudaSuccess;
-  if (g.kv_dtype != 0) return cudaErrorNotSupported;  // e4m3 prefill is not built yet
-  if (g.d == 128) return launch_t<128>(g, p, layer, q, kpool, vpool, out, lse, part_acc, part_ml, err, st);
-  if (g.d == 64) return launch_t<64>(g, p, layer, q, kpool, vpool, out, lse, part_acc, part_ml, err, st);
+  if (g.kv_dtype != 0) {
+    if (g.d != 128) return cudaErrorInvalidValue;
+    return launch_t<128, true>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st);
+  }
+  if (g.d == 128)
+    return launch_t<128, false>(g, p, layer, q, kpool, vpool, nullptr, nullptr, out, lse, part_acc, part_ml, err, st);
+  if (g.d == 64)
+    return launch_t<64, false>(g, p, layer, q, kpool, vpool, nullptr, nullptr, out, lse, part_acc, part_ml, err, st);
   return cudaErrorInvalidValue;
 }
 

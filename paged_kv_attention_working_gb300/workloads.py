@@ -226,7 +226,7 @@ def llama70b_fp8(**kw) -> Workload:
 
 
 def fork_spec(name="fork_spec", seed=3, prompt=4096, n_forks=10, suffix_hi=256, drafts=4,
-              rollback=2, num_layers=1, hq=32, hkv=8, d=128, unshared=True) -> Workload:
+              rollback=2, num_layers=1, hq=32, hkv=8, d=128, unshared=True, kv_dtype=KV_BF16) -> Workload:
     """One frozen prompt forked into n_forks working sets; each adds a frozen
     suffix of 1..suffix_hi tokens and `drafts` speculative tokens that are
     attended causally; then `rollback` drafts are dropped and re-appended
@@ -235,7 +235,7 @@ def fork_spec(name="fork_spec", seed=3, prompt=4096, n_forks=10, suffix_hi=256, 
     r = rng_for(seed, 0)
     suffix = r.integers(1, suffix_hi + 1, n_forks).tolist()
     ops = []
-    w = Workload(name, seed, num_layers, hq, hkv, d, KV_BF16, 0, ops)
+    w = Workload(name, seed, num_layers, hq, hkv, d, kv_dtype, 0, ops)
     w.kv_streams["prompt"] = prompt
     for i in range(n_forks):
         w.kv_streams[f"suf{i}"] = suffix[i]
@@ -274,7 +274,7 @@ def fork_spec(name="fork_spec", seed=3, prompt=4096, n_forks=10, suffix_hi=256, 
 
 def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=2048,
                 ctx_lo=0, ctx_hi=4096, n_decode=128, dec_lo=1, dec_hi=4096,
-                num_layers=1, hq=32, hkv=8, d=128) -> Workload:
+                num_layers=1, hq=32, hkv=8, d=128, kv_dtype=KV_BF16) -> Workload:
     """Mixed continuous batch: n_chunks prefill chunks of chunk_lo..chunk_hi new
     tokens on existing contexts of ctx_lo..ctx_hi tokens, plus n_decode
     single-token rows on contexts of dec_lo..dec_hi tokens, one attend call."""
@@ -283,7 +283,7 @@ def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=
     cctx = r.integers(ctx_lo, ctx_hi + 1, n_chunks).tolist()
     dctx = r.integers(dec_lo, dec_hi + 1, n_decode).tolist()
     ops = []
-    w = Workload(name, seed, num_layers, hq, hkv, d, KV_BF16, 0, ops)
+    w = Workload(name, seed, num_layers, hq, hkv, d, kv_dtype, 0, ops)
     fill, main = [], []
     for i in range(n_chunks):
         ops.append(("create", f"c{i}"))
@@ -308,7 +308,9 @@ def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=
 
 
 # The five workloads at full size (the parity tests also run reduced-size
-# variants of 2-5 that the oracle finishes in seconds).
+# variants of 2-5 that the oracle finishes in seconds, and e4m3-KV variants
+# of the fork and mixed workloads, which take the tensor-core path with
+# e4m3 pages).
 FULL = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
@@ -316,6 +318,9 @@ FULL = {
     "mixed_batch": mixed_batch,
     "llama70b_fp8": llama70b_fp8,
 }
+
+# Reduced-only variants: the same structure with e4m3 KV.
+EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3")
 
 
 def reduced(name: str) -> Workload:
@@ -332,6 +337,12 @@ def reduced(name: str) -> Workload:
     if name == "mixed_batch":
         return mixed_batch(name="mixed_batch_small", seed=14, n_chunks=3, chunk_lo=100, chunk_hi=300,
                            ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400)
+    if name == "fork_spec_e4m3":
+        return fork_spec(name="fork_spec_e4m3_small", seed=16, prompt=600, n_forks=10, suffix_hi=40,
+                         kv_dtype=KV_E4M3)
+    if name == "mixed_batch_e4m3":
+        return mixed_batch(name="mixed_batch_e4m3_small", seed=17, n_chunks=3, chunk_lo=100, chunk_hi=300,
+                           ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, kv_dtype=KV_E4M3)
     if name == "llama70b_fp8":
         return decode_batch(name="llama70b_fp8_small", seed=15, n_ws=8, ctx_lo=300, ctx_hi=1200,
                             num_layers=1, hq=64, hkv=8, d=128, kv_dtype=KV_E4M3,

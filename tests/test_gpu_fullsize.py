@@ -1,6 +1,6 @@
-"""GPU parity at the full sizes of the five workloads, in the launch
-configuration the benchmark times (the whole batch in one pie_batch /
-pie_attend per layer).
+"""GPU parity at the full sizes of the five workloads (and of the fork and
+mixed workloads with e4m3 KV), in the launch configuration the benchmark
+times (the whole batch in one pie_batch / pie_attend per layer).
 
 The oracle cannot hold every working set of the larger workloads, so a few
 working sets are sampled: their K/V/Q (and, for fork / dedup groups, the
@@ -153,14 +153,16 @@ def test_llama8b_decode_full():
     check(w, names, layers=[0, w.num_layers - 1])
 
 
-def test_fork_spec_full():
-    w = wl.fork_spec()
+@pytest.mark.parametrize("kv_dtype", [wl.KV_BF16, wl.KV_E4M3])
+def test_fork_spec_full(kv_dtype):
+    w = wl.fork_spec(kv_dtype=kv_dtype)
     names = ["root"] + [f"f{i}" for i in range(10)] + [f"u{i}" for i in range(10)]
     check(w, names, layers=[0])
 
 
-def test_mixed_batch_full():
-    w = wl.mixed_batch()
+@pytest.mark.parametrize("kv_dtype", [wl.KV_BF16, wl.KV_E4M3])
+def test_mixed_batch_full(kv_dtype):
+    w = wl.mixed_batch(kv_dtype=kv_dtype)
     chunks = list(np.argsort(w.chunks))
     names = [f"c{chunks[0]}", f"c{chunks[-1]}", "d0", "d77"]
     rng = np.random.default_rng(0)

@@ -39,7 +39,7 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("name", list(wl.FULL))
+@pytest.mark.parametrize("name", list(wl.FULL) + list(wl.EXTRA))
 def test_reduced_workload_parity(name):
     w = wl.reduced(name)
     store, handles, ref_passes = oracle_driver.run(w)

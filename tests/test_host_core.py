@@ -106,7 +106,7 @@ def test_random_operation_sequences_bit_exact():
         t.close()
 
 
-@pytest.mark.parametrize("name", list(wl.FULL))
+@pytest.mark.parametrize("name", list(wl.FULL) + list(wl.EXTRA))
 def test_workload_scripts_bit_exact(name):
     w = wl.reduced(name)
     c = pie.pie_ctx_create(w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages,
