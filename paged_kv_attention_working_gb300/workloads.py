@@ -67,6 +67,7 @@ class Workload:
     q_streams: dict = field(default_factory=dict)      # name -> length
     tok_streams: dict = field(default_factory=dict)    # name -> length
     page_size: int = 16
+    logit_softcap: float = 0.0     # > 0: scores capped at c * tanh(s / c)
     _cache: dict = field(default_factory=dict, repr=False)
 
     # --------------------------------------------------------------- inputs

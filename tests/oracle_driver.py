@@ -48,7 +48,8 @@ def run(w, layers=None, with_pool=True, compute=True, store=None, on_pass=None, 
                     k, v, q = w.pass_inputs(segs, layer, attend and layer in layers)
                     store.kv_append(pas, layer, k, v)
                     if attend and layer in layers:
-                        o, l = attention.attend_pass(store, pas, layer, kvstore.bf16_bits_to_f64(q))
+                        o, l = attention.attend_pass(store, pas, layer, kvstore.bf16_bits_to_f64(q),
+                                                    w.logit_softcap)
                         rec["out"][layer], rec["lse"][layer] = o, l
             if on_pass is not None:
                 on_pass(store, handles, rec)

@@ -186,3 +186,65 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(attention, "softmax_attention", transposed_pv)
     with pytest.raises(Exception):
         np.testing.assert_allclose(attention.attend_row(q, k, v, 5)[0], bo)
+
+
+# ---------------------------------------------------------------- logit soft cap
+# The pages name ``logit_softcap`` without a formula; the oracle reads it as
+# s <- c * tanh(s / c) on the scaled scores.  These pins come from limits and
+# one exactly solvable case, not from the formula restated.
+
+def test_softcap_large_cap_is_no_cap():
+    rng = np.random.default_rng(5)
+    q, k, v = rng.standard_normal(16), rng.standard_normal((9, 16)), rng.standard_normal((9, 16))
+    o0, l0 = attention.softmax_attention(q, k, v)
+    o1, l1 = attention.softmax_attention(q, k, v, softcap=1e7)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    assert abs(l1 - l0) < 1e-12
+
+
+def test_softcap_vanishing_cap_gives_mean_of_values():
+    """|capped score| <= c, so as c -> 0 every visible key weighs the same."""
+    rng = np.random.default_rng(6)
+    q, k, v = rng.standard_normal(8) * 4, rng.standard_normal((7, 8)), rng.standard_normal((7, 8))
+    c = 1e-9
+    o, lse = attention.softmax_attention(q, k, v, softcap=c)
+    np.testing.assert_allclose(o, v.mean(axis=0), rtol=0, atol=1e-8)
+    assert abs(lse - math.log(7)) < 1e-8
+
+
+def test_softcap_exact_case():
+    """d = 4 (scale 1/2), cap 2: a key with q.k = 2 ln 3 has scaled score ln 3,
+    capped to 2 tanh(ln 3 / 2) = 1 exactly; a zero key scores 0.  So the
+    weights are (1, e) / (1 + e) and lse = ln(1 + e)."""
+    q = np.array([2 * math.log(3), 0, 0, 0])
+    k = np.array([[0.0, 0, 0, 0], [1.0, 0, 0, 0]])
+    v = np.array([[1.0, 2, 3, 4], [-1.0, 0, 5, 2]])
+    o, lse = attention.softmax_attention(q, k, v, softcap=2.0)
+    e = math.e
+    np.testing.assert_allclose(o, (v[0] + e * v[1]) / (1 + e), rtol=1e-14, atol=1e-14)
+    assert abs(lse - math.log(1 + e)) < 1e-14
+    # the cap must act on the scaled score: capping q.k before the 1/sqrt(d)
+    # would give tanh(ln 3) = 0.8, and capping without the outer c would give 0.5
+    for wrong in (0.8, 0.5):
+        assert abs(lse - math.log(1 + math.exp(wrong))) > 1e-3
+
+
+def test_softcap_reaches_rows_of_a_pass():
+    """Every row of a pass (context plus a causal chunk) takes the cap: with a
+    vanishing cap each row is the mean of the values it may see."""
+    rng = np.random.default_rng(9)
+    hq, hkv, d, n_ctx, n_new = 4, 2, 64, 20, 6
+    kb = wl.bf16_round(rng.standard_normal((n_ctx + n_new, hkv, d)).astype(np.float32))
+    vb = wl.bf16_round(rng.standard_normal((n_ctx + n_new, hkv, d)).astype(np.float32))
+    qb = wl.bf16_round(rng.standard_normal((n_new, hq, d)).astype(np.float32))
+    st = kvstore.KVStore(1, hq, hkv, d, 4)
+    h = st.ws_create()
+    p0 = st.begin([(h, n_ctx, None)])
+    st.kv_append(p0, 0, kb[:n_ctx], vb[:n_ctx])
+    p1 = st.begin([(h, n_new, None)])
+    st.kv_append(p1, 0, kb[n_ctx:], vb[n_ctx:])
+    o, _ = attention.attend_pass(st, p1, 0, kvstore.bf16_bits_to_f64(qb), softcap=1e-9)
+    v = kvstore.bf16_bits_to_f64(vb)
+    for r, pos in enumerate(p1.rows_pos):
+        for hh in range(hq):
+            np.testing.assert_allclose(o[r, hh], v[:pos + 1, hh // 2].mean(axis=0), rtol=0, atol=1e-7)
