@@ -257,7 +257,8 @@ def run_gpu(args, w, world, rank, local):
     vpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
     ks, vs = w.scales()
     ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
-                             k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
+                             k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream,
+                             logit_softcap=args.logit_softcap)
     # set-up: every operation of the workload before its final (decode) pass,
     # with random bf16 K/V generated on the device
     gen = torch.Generator(device=dev)
@@ -385,6 +386,7 @@ def run_gpu(args, w, world, rank, local):
                    "layers": L,
                    "hq": Hq, "hkv": Hkv, "head_dim": D, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
                    "page_size": 16, "l2": "inputs larger than L2 (~1.1 GB KV per layer)",
+                   "logit_softcap": args.logit_softcap,
                    "parallelism": f"replicas x{world}"},
         "rows_per_s": world * n_rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
@@ -422,7 +424,8 @@ def run_mixed(args, w, world, rank, local):
     ks, vs = w.scales()
     ctx = pie.pie_ctx_create(w.num_layers, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype,
                              free_list=w.free_list().tolist(), k_scale=ks, v_scale=vs,
-                             k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream)
+                             k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream,
+                             logit_softcap=args.logit_softcap)
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000 + rank)
     hs = {}
@@ -490,6 +493,7 @@ def run_mixed(args, w, world, rank, local):
            "dtype": "bf16" if w.kv_dtype == 0 else "e4m3 KV as f16 operands, f16 Q/P, fp32 accumulate",
            "data": "synthetic",
            "config": {"workload": w.name, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
+                      "logit_softcap": args.logit_softcap,
                       "chunks": len(chunk_segs), "chunk_rows": sum(s[1] for s in chunk_segs),
                       "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1},
            "roofline": {"bound": "tensor", "kernel": "prefill_kernel (chunks-only attend)", "achieved": tflops,
@@ -517,6 +521,8 @@ def main():
                     choices=["llama8b_decode", "mixed_batch", "mixed_batch_e4m3", "llama70b_fp8"])
     ap.add_argument("--n-ws", type=int, default=0,
                     help="working sets of the e4m3 workload (0 = the full 256; fewer only for profiling)")
+    ap.add_argument("--logit-softcap", type=float, default=0.0,
+                    help="logit soft cap c of the attention scores (0 = none)")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
     args = ap.parse_args()

@@ -92,6 +92,11 @@ typedef struct pie_config {
                             device work; pie_kv_append / pie_attend fail) */
   void* v_pool;
   void* stream;          /* cudaStream_t, borrowed; NULL = legacy default */
+  float logit_softcap;   /* ops.attn.logit_softcap ("Poem ops"): c > 0 replaces
+                            every scaled score s by c * tanh(s / c) before the
+                            softmax (the LSE is over the capped scores);
+                            0 = no cap; negative or non-finite is
+                            PIE_ERR_INVALID */
 } pie_config;
 
 /* One segment of a pass: n_new new tokens of working set ws.  token_ids

@@ -17,7 +17,9 @@
 // thinks", section 4: the prompt is computed once and shared).
 //
 // E4M3 pages are converted in registers to f16 (exact) and the per-head
-// scales are folded into the softmax and output scaling.
+// scales are folded into the softmax and output scaling.  With a logit soft
+// cap (CAP) each visible score s becomes c * tanh(s / c) before the running
+// max and the exponentials.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,7 +49,7 @@ struct DecodeCfg {
   static constexpr int kSmem = (kRing > kCombineFloats * 4 ? kRing : kCombineFloats * 4) + 2 * kStages * 8 + 16;
 };
 
-template <bool E4M3, int D>
+template <bool E4M3, int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanView p, int layer,
                                                           const __nv_bfloat16* __restrict__ q,
                                                           const uint8_t* __restrict__ kpool,
@@ -104,7 +106,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
   const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group / thread in quad
   const float kdq = E4M3 ? kscale[layer * g.hkv + head] : 1.0f;
   const float vdq = E4M3 ? vscale[layer * g.hkv + head] : 1.0f;
+  // scores in log2 units: s * qk_scale, or with the soft cap c,
+  // tanh(s * cap_pre) * cap_post = c * tanh(s / c) * log2(e)
   const float qk_scale = kdq * rsqrtf(static_cast<float>(D)) * 1.4426950408889634f;
+  const float cap_pre = CAP ? kdq * rsqrtf(static_cast<float>(D)) / g.softcap : 0.f;
+  const float cap_post = CAP ? g.softcap * 1.4426950408889634f : 0.f;
 
   // the two M rows this thread holds: m = 16*mt + gq (+8)
   int mrow[2], mpos[2];
@@ -202,7 +208,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           int kpos = kbase + nt * 8 + 2 * tq + e;
-          float v = kpos <= mpos[h] ? sc[nt][2 * h + e] * qk_scale : -INFINITY;
+          float v;
+          if constexpr (CAP)
+            v = kpos <= mpos[h] ? tanh_approx(sc[nt][2 * h + e] * cap_pre) * cap_post : -INFINITY;
+          else
+            v = kpos <= mpos[h] ? sc[nt][2 * h + e] * qk_scale : -INFINITY;
           sc[nt][2 * h + e] = v;
           best = fmaxf(best, v);
         }
@@ -390,19 +400,20 @@ __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__
   if (lse && lane == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (m + __log2f(l)) * 0.6931471805599453f;
 }
 
-template <bool E4M3, int D>
+template <bool E4M3, int D, bool CAP = false>
 cudaError_t launch_decode_t(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
                             const void* vpool, const float* ks, const float* vs, void* out, float* lse,
                             float* acc, float* ml, int* err, cudaStream_t st) {
   using C = DecodeCfg<E4M3, D>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<E4M3, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<E4M3, D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   dim3 grid(p.n_dec, g.hkv);
-  decode_kernel<E4M3, D><<<grid, kThreads, C::kSmem, st>>>(
+  decode_kernel<E4M3, D, CAP><<<grid, kThreads, C::kSmem, st>>>(
       g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
       static_cast<const uint8_t*>(vpool), ks, vs, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
   return cudaGetLastError();
@@ -414,15 +425,13 @@ cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const
                           const void* vpool, const float* scale_k, const float* scale_v, void* out, float* lse,
                           float* part_acc, float* part_ml, int* err, cudaStream_t st) {
   if (p.n_dec == 0) return cudaSuccess;
-  if (g.kv_dtype == 0 && g.d == 128)
-    return launch_decode_t<false, 128>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml,
-                                       err, st);
-  if (g.kv_dtype == 0 && g.d == 64)
-    return launch_decode_t<false, 64>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml,
-                                      err, st);
-  if (g.kv_dtype == 1 && g.d == 128)
-    return launch_decode_t<true, 128>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml,
-                                      err, st);
+#define PIE_DECODE(E, DD, CP) \
+  launch_decode_t<E, DD, CP>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st)
+  const bool cap = g.softcap > 0.f;
+  if (g.kv_dtype == 0 && g.d == 128) return cap ? PIE_DECODE(false, 128, true) : PIE_DECODE(false, 128, false);
+  if (g.kv_dtype == 0 && g.d == 64) return cap ? PIE_DECODE(false, 64, true) : PIE_DECODE(false, 64, false);
+  if (g.kv_dtype == 1 && g.d == 128) return cap ? PIE_DECODE(true, 128, true) : PIE_DECODE(true, 128, false);
+#undef PIE_DECODE
   return cudaErrorInvalidValue;
 }
 

@@ -10,6 +10,7 @@
 // ops", Operations table).
 #include <algorithm>
 #include <array>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -383,11 +384,12 @@ pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out) {
   if (!dim_ok || G > 64 || (G & (G - 1))) return PIE_ERR_INVALID;
   if ((k.k_pool == nullptr) != (k.v_pool == nullptr)) return PIE_ERR_INVALID;
   if (k.kv_dtype == PIE_KV_E4M3 && (!k.k_scale || !k.v_scale)) return PIE_ERR_INVALID;
+  if (!(k.logit_softcap >= 0.0f) || !std::isfinite(k.logit_softcap)) return PIE_ERR_INVALID;
 
   auto* c = new pie_ctx();
   c->cfg = k;
   c->geo = {k.num_layers, k.num_q_heads, k.num_kv_heads, k.head_dim, k.num_pages, k.kv_dtype,
-            static_cast<int64_t>(kPageSize) * k.head_dim * esize};
+            static_cast<int64_t>(kPageSize) * k.head_dim * esize, k.logit_softcap};
   c->plan_only = k.k_pool == nullptr;
   c->stream = static_cast<cudaStream_t>(k.stream);
   c->refcount.assign(k.num_pages, 0);

@@ -47,6 +47,7 @@ struct PlanView {
 struct Geometry {
   int32_t num_layers, hq, hkv, d, num_pages, kv_dtype;
   int64_t block_bytes;  // 16 * d * esize
+  float softcap;        // > 0: scores s become softcap * tanh(s / softcap)
 };
 
 // Kernel launchers (defined in the .cu files); all return cudaGetLastError().

@@ -29,6 +29,10 @@
 // Rows with one part are normalised and written as bf16; otherwise the
 // fp32 (acc, m, l) partial goes to the merge kernel.
 //
+// With a logit soft cap c (CAP), the softmax warps map each raw score to
+// tanh(s * scale / c) before masking, and c * log2(e) takes the place of the
+// score scale.
+//
 // e4m3 pools (d = 128): the tensor cores take the dequantised codes.  The
 // producer copies raw e4m3 page blocks into a small staging ring; two
 // converter warps turn each 16-key page into f16 (every e4m3 value is exact
@@ -145,7 +149,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool E4M3>
+template <int D, bool E4M3, bool CAP>
 __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     prefill_kernel(Geometry g, PlanView p, int layer, const __nv_bfloat16* __restrict__ q,
                    const uint8_t* __restrict__ kpool, const uint8_t* __restrict__ vpool,
@@ -418,8 +422,12 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
       pos = p.row_pos[row];
       qh = head * G + m % G;
     }
-    const float qk_scale = (E4M3 ? kscale[layer * g.hkv + head] : 1.0f) * 1.4426950408889634f *
-                           rsqrtf(static_cast<float>(D));
+    // scores in log2 units: s * qk_scale; with the soft cap c the scores
+    // are first mapped to tanh(s * cap_pre) and then scaled by
+    // qk_scale = c * log2(e) (c * tanh(s / c) in log2 units)
+    const float s_scale = (E4M3 ? kscale[layer * g.hkv + head] : 1.0f) * rsqrtf(static_cast<float>(D));
+    const float qk_scale = CAP ? g.softcap * 1.4426950408889634f : s_scale * 1.4426950408889634f;
+    const float cap_pre = CAP ? s_scale / g.softcap : 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
@@ -438,6 +446,10 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < C::kKeys / 32; ++c) tc::ld32(row_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
       tc::wait_ld();
+      if constexpr (CAP) {
+#pragma unroll
+        for (int e = 0; e < C::kKeys; ++e) sr[e] = __float_as_uint(tanh_approx(__uint_as_float(sr[e]) * cap_pre));
+      }
       if (masked) {
 #pragma unroll
         for (int e = 0; e < C::kKeys; ++e)
@@ -538,7 +550,7 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
   }
 }
 
-template <int D, bool E4M3>
+template <int D, bool E4M3, bool CAP>
 cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
                      const void* vpool, const float* kscale, const float* vscale, void* out, float* lse, float* acc,
                      float* ml, int* err, cudaStream_t st) {
@@ -547,12 +559,12 @@ cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D, E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(prefill_kernel<D, E4M3, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   dim3 grid(p.n_pre, g.hkv);
-  prefill_kernel<D, E4M3><<<grid, C::kThreads, C::kSmem, st>>>(
+  prefill_kernel<D, E4M3, CAP><<<grid, C::kThreads, C::kSmem, st>>>(
       g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
       static_cast<const uint8_t*>(vpool), kscale, vscale, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
   return cudaGetLastError();
@@ -564,14 +576,16 @@ cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, cons
                            const void* vpool, const float* scale_k, const float* scale_v, void* out, float* lse,
                            float* part_acc, float* part_ml, int* err, cudaStream_t st) {
   if (p.n_pre == 0) return cudaSuccess;
+#define PIE_PREFILL(DD, E, CP) \
+  launch_t<DD, E, CP>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st)
+  const bool cap = g.softcap > 0.f;
   if (g.kv_dtype != 0) {
     if (g.d != 128) return cudaErrorInvalidValue;
-    return launch_t<128, true>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st);
+    return cap ? PIE_PREFILL(128, true, true) : PIE_PREFILL(128, true, false);
   }
-  if (g.d == 128)
-    return launch_t<128, false>(g, p, layer, q, kpool, vpool, nullptr, nullptr, out, lse, part_acc, part_ml, err, st);
-  if (g.d == 64)
-    return launch_t<64, false>(g, p, layer, q, kpool, vpool, nullptr, nullptr, out, lse, part_acc, part_ml, err, st);
+  if (g.d == 128) return cap ? PIE_PREFILL(128, false, true) : PIE_PREFILL(128, false, false);
+  if (g.d == 64) return cap ? PIE_PREFILL(64, false, true) : PIE_PREFILL(64, false, false);
+#undef PIE_PREFILL
   return cudaErrorInvalidValue;
 }
 

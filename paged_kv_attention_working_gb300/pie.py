@@ -48,6 +48,7 @@ class pie_config(ctypes.Structure):
         ("free_list", ctypes.POINTER(ctypes.c_int32)),
         ("k_scale", ctypes.POINTER(ctypes.c_float)), ("v_scale", ctypes.POINTER(ctypes.c_float)),
         ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("stream", ctypes.c_void_p),
+        ("logit_softcap", ctypes.c_float),
     ]
 
 
@@ -132,7 +133,7 @@ def _check(ctx, st: int, what: str) -> None:
 # ------------------------------------------------------------------ context
 def pie_ctx_create(num_layers, num_q_heads, num_kv_heads, head_dim, num_pages, kv_dtype=PIE_KV_BF16,
                    free_list=None, k_scale=None, v_scale=None, k_pool=None, v_pool=None, stream=None,
-                   num_sms=0, page_size=16):
+                   num_sms=0, page_size=16, logit_softcap=0.0):
     """Returns an opaque context handle (int).  k_pool/v_pool None = plan-only."""
     keep = []
     cfg = pie_config()
@@ -151,6 +152,7 @@ def pie_ctx_create(num_layers, num_q_heads, num_kv_heads, head_dim, num_pages, k
             setattr(cfg, field, ctypes.cast(arr, ctypes.POINTER(ctypes.c_float)))
     cfg.k_pool, cfg.v_pool = _ptr(k_pool), _ptr(v_pool)
     cfg.stream = _ptr(stream)
+    cfg.logit_softcap = logit_softcap
     out = ctypes.c_void_p()
     st = lib.pie_ctx_create(ctypes.byref(cfg), ctypes.byref(out))
     if st != PIE_OK:

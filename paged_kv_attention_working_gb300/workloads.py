@@ -320,14 +320,22 @@ FULL = {
     "llama70b_fp8": llama70b_fp8,
 }
 
-# Reduced-only variants: the same structure with e4m3 KV.
-EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3")
+# Reduced-only variants: the same structure with e4m3 KV, and with a logit
+# soft cap of 3 (small enough that the cap bends N(0,1) scores visibly).
+EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_batch_e4m3_softcap",
+         "llama70b_fp8_softcap", "tiny_decode_softcap", "fork_spec_softcap")
+SOFTCAP_TEST = 3.0
 
 
 def reduced(name: str) -> Workload:
     """Oracle-sized variant of a full workload: same structure and head shapes,
     fewer working sets and shorter contexts, still several pages, splits and
     MMA tiles long with ragged tails."""
+    if name.endswith("_softcap"):
+        w = reduced(name[: -len("_softcap")])
+        w.name += "_softcap"
+        w.logit_softcap = SOFTCAP_TEST
+        return w
     if name == "tiny_decode":
         return tiny_decode()
     if name == "llama8b_decode":

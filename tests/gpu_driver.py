@@ -26,7 +26,7 @@ class GpuRun:
         self.ctx = pie.pie_ctx_create(w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages,
                                       kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(), k_scale=ks,
                                       v_scale=vs, k_pool=self.kpool, v_pool=self.vpool,
-                                      stream=self.stream.cuda_stream)
+                                      stream=self.stream.cuda_stream, logit_softcap=w.logit_softcap)
         self.handles = {}
 
     def run(self, layers=None, kv_source=None):

@@ -262,6 +262,9 @@ def test_invalid_configurations_rejected():
         pie.pie_ctx_create(1, 4, 2, 128, 8, kv_dtype=pie.PIE_KV_E4M3)   # e4m3 without scales
     with pytest.raises(pie.PieError):
         pie.pie_ctx_create(1, 4, 2, 64, 4, free_list=[0, 1, 1, 2])      # not a permutation
+    for cap in (-1.0, float("inf"), float("nan")):
+        with pytest.raises(pie.PieError):
+            pie.pie_ctx_create(1, 4, 2, 64, 8, logit_softcap=cap)       # soft cap must be finite, >= 0
 
 
 def test_plan_prefill_chunks_never_join_groups():

@@ -162,7 +162,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
     v = rng.standard_normal((6, 2, 8))
     bo, _ = brute_force_row(q.tolist(), k.tolist(), v.tolist(), 5)
 
-    def no_scale(q, k, v):
+    def no_scale(q, k, v, softcap=0.0):
         s = np.asarray(k) @ np.asarray(q)
         e = np.exp(s - s.max())
         return (e @ np.asarray(v)) / e.sum(), 0.0
@@ -174,17 +174,18 @@ def test_planted_mistakes_are_caught(monkeypatch):
             o[h], _ = attention.softmax_attention(q_row[h], k_ctx[:pos + 1, h % 2], v_ctx[:pos + 1, h % 2])
         return o, None
 
-    def transposed_pv(q, k, v):
+    def reversed_keys(q, k, v, softcap=0.0):
+        # weights paired with the values in reverse order (an index mistake)
         s = (np.asarray(k) @ np.asarray(q)) / np.sqrt(len(q))
         e = np.exp(s - s.max())
-        return (np.asarray(v)[:len(q)] @ e[:len(q)]) / e.sum() if len(q) <= len(e) else e, 0.0
+        return (e[::-1] @ np.asarray(v)) / e.sum(), 0.0
 
     monkeypatch.setattr(attention, "softmax_attention", no_scale)
     assert not np.allclose(attention.attend_row(q, k, v, 5)[0], bo)
     monkeypatch.undo()
     assert not np.allclose(wrong_group(q, k, v, 5)[0], bo)
-    monkeypatch.setattr(attention, "softmax_attention", transposed_pv)
-    with pytest.raises(Exception):
+    monkeypatch.setattr(attention, "softmax_attention", reversed_keys)
+    with pytest.raises(AssertionError):
         np.testing.assert_allclose(attention.attend_row(q, k, v, 5)[0], bo)
 
 
