@@ -20,6 +20,9 @@ the CUDA library.  The modules:
 * ``attention`` -- exact softmax(q K^T / sqrt(d)) V per query row over the
                    row's working set, with grouped-query head mapping and the
                    causal rule, computed from keys gathered out of the store.
+* ``rope``      -- the rotary position embedding of new K (and Q) rows that
+                   precedes the append, in the kernel's float32 precision,
+                   with the float64 rotation it is pinned against.
 
 Parity status per function is listed in each module's docstring.
 """
