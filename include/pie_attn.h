@@ -97,6 +97,11 @@ typedef struct pie_config {
                             softmax (the LSE is over the capped scores);
                             0 = no cap; negative or non-finite is
                             PIE_ERR_INVALID */
+  float rope_theta;      /* > 1: the context builds the rotary table of
+                            pie_rope_table(rope_theta, head_dim,
+                            rope_max_positions) on the device for
+                            pie_kv_append_rope; 0 = none */
+  int32_t rope_max_positions; /* positions the table covers (rope_theta > 0) */
 } pie_config;
 
 /* One segment of a pass: n_new new tokens of working set ws.  token_ids
@@ -169,6 +174,26 @@ pie_status pie_batch_slots(const pie_batch* b, int32_t* pos, int32_t* slot);
  * an e4m3 context). */
 pie_status pie_kv_append(pie_ctx* ctx, pie_batch* b, int32_t layer,
                          const void* k, const void* v);
+/* ops.elemwise.rope fused into ops.attn.kv_append ("Poem ops", Operations
+ * table; the pages name the op without a formula, and the rotary embedding
+ * of the Llama family is taken): for each row at position p, dimension i <
+ * d/2 of a head pairs with i + d/2 and both turn by the angle p * w_i,
+ * w_i = rope_theta^(-2i/d):
+ *     y_i = x_i cos - x_{i+d/2} sin,   y_{i+d/2} = x_{i+d/2} cos + x_i sin,
+ * with (cos, sin) from the context's table, each product and the sum in
+ * float32 (no fused multiply-add), rounded to bf16.  K heads are rotated and
+ * appended exactly as pie_kv_append would append the rotated bf16 rows (V is
+ * appended unrotated); when q is non-NULL, q [n_rows][Hq][d] bf16 is rotated
+ * into q_out (same layout; q_out may equal q) for the following pie_attend.
+ * PIE_ERR_STATE if the context has no rotary table; PIE_ERR_RANGE, with
+ * nothing launched, if a row position is >= rope_max_positions. */
+pie_status pie_kv_append_rope(pie_ctx* ctx, pie_batch* b, int32_t layer, const void* k, const void* v,
+                              const void* q, void* q_out);
+/* Host: the rotary table, out [positions][head_dim/2][2] float = (cos, sin)
+ * of p * theta^(-2i/head_dim), each computed in double and rounded to float.
+ * theta > 1, head_dim even, positions > 0, else PIE_ERR_INVALID. */
+pie_status pie_rope_table(float theta, int32_t head_dim, int32_t positions, float* out);
+
 /* ops.attn.attend / prefill for one layer: q device bf16 [n_rows][Hq][d];
  * out device bf16 [n_rows][Hq][d]; lse device float [n_rows][Hq] (natural
  * log of the softmax denominator) or NULL.  Row r at position p of working

@@ -83,6 +83,111 @@ __global__ void kv_append_e4m3(Geometry g, PlanView p, int layer, const uint4* _
   *reinterpret_cast<uint4*>(vpool + off) = vo;
 }
 
+// ---------------------------------------------------------------- rope
+// Rotary embedding fused into the append ("Poem ops": ops.elemwise.rope
+// feeding ops.attn.kv_append): dimension i of a head pairs with i + d/2 and
+// turns by the row position's angle from the (cos, sin) table,
+//   y_i = x_i c - x_{i+d/2} s,   y_{i+d/2} = x_{i+d/2} c + x_i s,
+// each product and the sum rounded to float32 (no fused multiply-add), the
+// result rounded to bf16 -- the same bytes as rotating to bf16 first and
+// appending after.  One thread takes 16 dimensions of each half of one head
+// of one row: K heads (rotated, then stored or quantised like
+// kv_append_bf16 / kv_append_e4m3, with their V unrotated), then, when q is
+// given, Q heads (rotated into q_out).
+
+// Rotates 8 bf16 pairs: a holds dims j..j+7 of the first half, b the same of
+// the second half, cs the 8 (cos, sin) pairs.
+__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float4* cs) {
+  uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
+  uint32_t* pb = reinterpret_cast<uint32_t*>(&b);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float4 t = __ldg(cs + w);  // (c0, s0, c1, s1) of the two dims in word w
+    float x0[2] = {__uint_as_float(pa[w] << 16), __uint_as_float(pa[w] & 0xFFFF0000u)};
+    float x1[2] = {__uint_as_float(pb[w] << 16), __uint_as_float(pb[w] & 0xFFFF0000u)};
+    const float c[2] = {t.x, t.z}, sn[2] = {t.y, t.w};
+    float y0[2], y1[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      y0[e] = __fsub_rn(__fmul_rn(x0[e], c[e]), __fmul_rn(x1[e], sn[e]));
+      y1[e] = __fadd_rn(__fmul_rn(x1[e], c[e]), __fmul_rn(x0[e], sn[e]));
+    }
+    const __nv_bfloat162 r0 = __floats2bfloat162_rn(y0[0], y0[1]);  // .x (low half) = first dim
+    const __nv_bfloat162 r1 = __floats2bfloat162_rn(y1[0], y1[1]);
+    pa[w] = *reinterpret_cast<const uint32_t*>(&r0);
+    pb[w] = *reinterpret_cast<const uint32_t*>(&r1);
+  }
+}
+
+template <bool E4M3>
+__global__ void kv_append_rope(Geometry g, PlanView p, int layer, const uint4* __restrict__ k,
+                               const uint4* __restrict__ v, const uint4* __restrict__ q, uint4* __restrict__ q_out,
+                               const float* __restrict__ rope, uint8_t* __restrict__ kpool,
+                               uint8_t* __restrict__ vpool, const float* __restrict__ inv_k,
+                               const float* __restrict__ inv_v) {
+  const int nc = g.d / 32;        // 16-dimension groups per half
+  const int hd = g.d / 8;         // 16-byte chunks per head row
+  const int heads = g.hkv + (q ? g.hq : 0);
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(p.n_rows) * heads * nc) return;
+  const int c = static_cast<int>(idx % nc);
+  const int64_t rh = idx / nc;
+  const int hh = static_cast<int>(rh % heads);
+  const int row = static_cast<int>(rh / heads);
+  const int pos = p.row_pos[row];
+  const float4* cs = reinterpret_cast<const float4*>(rope + (static_cast<int64_t>(pos) * (g.d / 2) + 16 * c) * 2);
+  // chunk indices (16-byte bf16 units) of the thread's dims in a head row
+  const int c0 = 2 * c, c1 = hd / 2 + 2 * c;
+  if (hh >= g.hkv) {
+    const int64_t base = (static_cast<int64_t>(row) * g.hq + (hh - g.hkv)) * hd;
+    uint4 a0 = __ldg(q + base + c0), a1 = __ldg(q + base + c0 + 1);
+    uint4 b0 = __ldg(q + base + c1), b1 = __ldg(q + base + c1 + 1);
+    rotate8(a0, b0, cs);
+    rotate8(a1, b1, cs + 4);
+    q_out[base + c0] = a0;
+    q_out[base + c0 + 1] = a1;
+    q_out[base + c1] = b0;
+    q_out[base + c1 + 1] = b1;
+    return;
+  }
+  const int head = hh;
+  const int64_t base = (static_cast<int64_t>(row) * g.hkv + head) * hd;
+  uint4 a0 = __ldg(k + base + c0), a1 = __ldg(k + base + c0 + 1);
+  uint4 b0 = __ldg(k + base + c1), b1 = __ldg(k + base + c1 + 1);
+  rotate8(a0, b0, cs);
+  rotate8(a1, b1, cs + 4);
+  const uint4 va0 = __ldg(v + base + c0), va1 = __ldg(v + base + c0 + 1);
+  const uint4 vb0 = __ldg(v + base + c1), vb1 = __ldg(v + base + c1 + 1);
+  const int slot = p.row_slot[row];
+  if constexpr (!E4M3) {
+    const int64_t o0 = slot_chunk_offset(g, layer, slot >> 4, head, slot & 15, c0);
+    const int64_t o1 = slot_chunk_offset(g, layer, slot >> 4, head, slot & 15, c0 + 1);
+    const int64_t o2 = slot_chunk_offset(g, layer, slot >> 4, head, slot & 15, c1);
+    const int64_t o3 = slot_chunk_offset(g, layer, slot >> 4, head, slot & 15, c1 + 1);
+    *reinterpret_cast<uint4*>(kpool + o0) = a0;
+    *reinterpret_cast<uint4*>(kpool + o1) = a1;
+    *reinterpret_cast<uint4*>(kpool + o2) = b0;
+    *reinterpret_cast<uint4*>(kpool + o3) = b1;
+    *reinterpret_cast<uint4*>(vpool + o0) = va0;
+    *reinterpret_cast<uint4*>(vpool + o1) = va1;
+    *reinterpret_cast<uint4*>(vpool + o2) = vb0;
+    *reinterpret_cast<uint4*>(vpool + o3) = vb1;
+  } else {
+    // e4m3 chunk e holds dims 16e..16e+15: this thread's are chunks c and d/32 + c
+    const float ik = inv_k[layer * g.hkv + head], iv = inv_v[layer * g.hkv + head];
+    const int64_t o0 = slot_chunk_offset(g, layer, slot >> 4, head, slot & 15, c);
+    const int64_t o1 = slot_chunk_offset(g, layer, slot >> 4, head, slot & 15, nc + c);
+    auto q16 = [](uint4 lo, uint4 hi, float inv) {
+      return make_uint4(quant4(make_uint2(lo.x, lo.y), inv), quant4(make_uint2(lo.z, lo.w), inv),
+                        quant4(make_uint2(hi.x, hi.y), inv), quant4(make_uint2(hi.z, hi.w), inv));
+    };
+    *reinterpret_cast<uint4*>(kpool + o0) = q16(a0, a1, ik);
+    *reinterpret_cast<uint4*>(kpool + o1) = q16(b0, b1, ik);
+    *reinterpret_cast<uint4*>(vpool + o0) = q16(va0, va1, iv);
+    *reinterpret_cast<uint4*>(vpool + o1) = q16(vb0, vb1, iv);
+  }
+}
+
 // copy-on-write: blockIdx.x = copy * layers + layer, blockIdx.y = K / V.
 // A page's blocks for all heads are contiguous, so one page of one layer is
 // hkv * block_bytes consecutive bytes.
@@ -114,6 +219,27 @@ cudaError_t launch_kv_append(const Geometry& g, const PlanView& p, int layer, co
     kv_append_e4m3<<<blocks, threads, 0, st>>>(g, p, layer, static_cast<const uint4*>(k),
                                                 static_cast<const uint4*>(v), static_cast<uint8_t*>(kpool),
                                                 static_cast<uint8_t*>(vpool), inv_scale_k, inv_scale_v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append_rope(const Geometry& g, const PlanView& p, int layer, const void* k, const void* v,
+                                  const void* q, void* q_out, const float* rope, void* kpool, void* vpool,
+                                  const float* inv_scale_k, const float* inv_scale_v, cudaStream_t st) {
+  const int heads = g.hkv + (q ? g.hq : 0);
+  int64_t total = static_cast<int64_t>(p.n_rows) * heads * (g.d / 32);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
+  auto args = [&](auto kern) {
+    kern<<<blocks, threads, 0, st>>>(g, p, layer, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                                     static_cast<const uint4*>(q), static_cast<uint4*>(q_out), rope,
+                                     static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool), inv_scale_k,
+                                     inv_scale_v);
+  };
+  if (g.kv_dtype == 0)
+    args(kv_append_rope<false>);
+  else
+    args(kv_append_rope<true>);
   return cudaGetLastError();
 }
 

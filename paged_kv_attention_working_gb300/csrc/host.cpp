@@ -90,6 +90,7 @@ struct pie_ctx {
 
   // device buffers owned by the context
   float* d_scales = nullptr;  // [4][L*Hkv]: k_scale, v_scale, 1/k_scale, 1/v_scale
+  float* d_rope = nullptr;    // [rope_max_positions][d/2][2] (cos, sin), when rope_theta > 0
   int* d_err = nullptr;       // error bits set by kernels (bounded waits that ran out)
   uint8_t* d_plan = nullptr;
   size_t plan_cap = 0;
@@ -385,6 +386,8 @@ pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out) {
   if ((k.k_pool == nullptr) != (k.v_pool == nullptr)) return PIE_ERR_INVALID;
   if (k.kv_dtype == PIE_KV_E4M3 && (!k.k_scale || !k.v_scale)) return PIE_ERR_INVALID;
   if (!(k.logit_softcap >= 0.0f) || !std::isfinite(k.logit_softcap)) return PIE_ERR_INVALID;
+  if (!(k.rope_theta >= 0.0f) || !std::isfinite(k.rope_theta)) return PIE_ERR_INVALID;
+  if (k.rope_theta > 0.0f && (k.rope_theta <= 1.0f || k.rope_max_positions <= 0)) return PIE_ERR_INVALID;
 
   auto* c = new pie_ctx();
   c->cfg = k;
@@ -440,6 +443,12 @@ pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&c->d_err), sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
+    if (e == cudaSuccess && k.rope_theta > 0.0f) {
+      std::vector<float> tab(static_cast<size_t>(k.rope_max_positions) * k.head_dim);
+      pie_rope_table(k.rope_theta, k.head_dim, k.rope_max_positions, tab.data());
+      e = cudaMalloc(reinterpret_cast<void**>(&c->d_rope), tab.size() * sizeof(float));
+      if (e == cudaSuccess) e = cudaMemcpy(c->d_rope, tab.data(), tab.size() * sizeof(float), cudaMemcpyHostToDevice);
+    }
     if (e != cudaSuccess) {
       pie_ctx_destroy(c);
       return PIE_ERR_CUDA;
@@ -454,6 +463,7 @@ pie_status pie_ctx_destroy(pie_ctx* c) {
   if (!c->plan_only) {
     cudaStreamSynchronize(c->stream);
     if (c->d_scales) cudaFree(c->d_scales);
+    if (c->d_rope) cudaFree(c->d_rope);
     if (c->d_err) cudaFree(c->d_err);
     if (c->d_plan) cudaFree(c->d_plan);
     if (c->d_part) cudaFree(c->d_part);
@@ -761,6 +771,41 @@ pie_status pie_kv_append(pie_ctx* c, pie_batch* b, int32_t layer, const void* k,
   cudaError_t e = pie::launch_kv_append(c->geo, b->view, layer, k, v, c->cfg.k_pool, c->cfg.v_pool,
                                         c->d_scales + 2 * nsc, c->d_scales + 3 * nsc, c->stream);
   if (e != cudaSuccess) return cuda_fail(c, e, "kv_append launch");
+  b->appended_any = true;
+  return PIE_OK;
+}
+
+pie_status pie_rope_table(float theta, int32_t head_dim, int32_t positions, float* out) {
+  if (!out || head_dim <= 0 || head_dim % 2 || positions <= 0 || !(theta > 1.0f) || !std::isfinite(theta))
+    return PIE_ERR_INVALID;
+  const int32_t half = head_dim / 2;
+  std::vector<double> w(half);
+  for (int32_t i = 0; i < half; ++i) w[i] = std::pow(static_cast<double>(theta), -2.0 * i / head_dim);
+  for (int32_t p = 0; p < positions; ++p)
+    for (int32_t i = 0; i < half; ++i) {
+      const double a = static_cast<double>(p) * w[i];
+      out[(static_cast<size_t>(p) * half + i) * 2] = static_cast<float>(std::cos(a));
+      out[(static_cast<size_t>(p) * half + i) * 2 + 1] = static_cast<float>(std::sin(a));
+    }
+  return PIE_OK;
+}
+
+pie_status pie_kv_append_rope(pie_ctx* c, pie_batch* b, int32_t layer, const void* k, const void* v, const void* q,
+                              void* q_out) {
+  if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
+  if (!c->d_rope) return fail(c, PIE_ERR_STATE, "context has no rotary table (rope_theta = 0)");
+  if (layer < 0 || layer >= c->geo.num_layers) return fail(c, PIE_ERR_INVALID, "layer %d", layer);
+  if (b->n_rows == 0) return PIE_OK;
+  if (!k || !v) return fail(c, PIE_ERR_INVALID, "null K or V");
+  if ((q == nullptr) != (q_out == nullptr)) return fail(c, PIE_ERR_INVALID, "q and q_out go together");
+  for (int32_t pos : b->row_pos)
+    if (pos >= c->cfg.rope_max_positions)
+      return fail(c, PIE_ERR_RANGE, "position %d beyond the rotary table (%d)", pos, c->cfg.rope_max_positions);
+  const int32_t nsc = c->geo.num_layers * c->geo.hkv;
+  cudaError_t e = pie::launch_kv_append_rope(c->geo, b->view, layer, k, v, q, q_out, c->d_rope, c->cfg.k_pool,
+                                             c->cfg.v_pool, c->d_scales + 2 * nsc, c->d_scales + 3 * nsc, c->stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "kv_append_rope launch");
   b->appended_any = true;
   return PIE_OK;
 }

@@ -55,6 +55,10 @@ cudaError_t launch_kv_append(const Geometry& g, const PlanView& p, int layer,
                              const void* k, const void* v, void* kpool, void* vpool,
                              const float* inv_scale_k, const float* inv_scale_v,
                              cudaStream_t st);
+cudaError_t launch_kv_append_rope(const Geometry& g, const PlanView& p, int layer, const void* k,
+                                  const void* v, const void* q, void* q_out, const float* rope,
+                                  void* kpool, void* vpool, const float* inv_scale_k,
+                                  const float* inv_scale_v, cudaStream_t st);
 cudaError_t launch_page_copy(const Geometry& g, const PlanView& p, void* kpool, void* vpool,
                              cudaStream_t st);
 cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const void* q,

@@ -30,6 +30,7 @@ EXPORTS = [
     "pie_ws_page_table", "pie_page_refcount", "pie_free_pages", "pie_batch_begin", "pie_batch_rows",
     "pie_batch_slots", "pie_kv_append", "pie_attend", "pie_batch_end", "pie_batch_plan_info",
     "pie_batch_items", "pie_ctx_check", "pie_attend_decode_noalloc", "pie_selftest_wait_timeout",
+    "pie_kv_append_rope", "pie_rope_table",
 ]
 PIE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -48,7 +49,8 @@ class pie_config(ctypes.Structure):
         ("free_list", ctypes.POINTER(ctypes.c_int32)),
         ("k_scale", ctypes.POINTER(ctypes.c_float)), ("v_scale", ctypes.POINTER(ctypes.c_float)),
         ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("stream", ctypes.c_void_p),
-        ("logit_softcap", ctypes.c_float),
+        ("logit_softcap", ctypes.c_float), ("rope_theta", ctypes.c_float),
+        ("rope_max_positions", ctypes.c_int32),
     ]
 
 
@@ -89,6 +91,8 @@ def _load():
         "pie_batch_rows": [V, P(I)],
         "pie_batch_slots": [V, P(I), P(I)],
         "pie_kv_append": [V, V, I, V, V],
+        "pie_kv_append_rope": [V, V, I, V, V, V, V],
+        "pie_rope_table": [F, I, I, P(F)],
         "pie_attend": [V, V, I, V, V, V],
         "pie_batch_end": [V, V],
         "pie_batch_plan_info": [V, P(I)],
@@ -133,7 +137,7 @@ def _check(ctx, st: int, what: str) -> None:
 # ------------------------------------------------------------------ context
 def pie_ctx_create(num_layers, num_q_heads, num_kv_heads, head_dim, num_pages, kv_dtype=PIE_KV_BF16,
                    free_list=None, k_scale=None, v_scale=None, k_pool=None, v_pool=None, stream=None,
-                   num_sms=0, page_size=16, logit_softcap=0.0):
+                   num_sms=0, page_size=16, logit_softcap=0.0, rope_theta=0.0, rope_max_positions=0):
     """Returns an opaque context handle (int).  k_pool/v_pool None = plan-only."""
     keep = []
     cfg = pie_config()
@@ -153,6 +157,7 @@ def pie_ctx_create(num_layers, num_q_heads, num_kv_heads, head_dim, num_pages, k
     cfg.k_pool, cfg.v_pool = _ptr(k_pool), _ptr(v_pool)
     cfg.stream = _ptr(stream)
     cfg.logit_softcap = logit_softcap
+    cfg.rope_theta, cfg.rope_max_positions = rope_theta, rope_max_positions
     out = ctypes.c_void_p()
     st = lib.pie_ctx_create(ctypes.byref(cfg), ctypes.byref(out))
     if st != PIE_OK:
@@ -283,6 +288,21 @@ def pie_batch_items(batch, kind):
 
 def pie_kv_append(ctx, batch, layer, k, v) -> None:
     _check(ctx, lib.pie_kv_append(ctx, batch, layer, _ptr(k), _ptr(v)), "pie_kv_append")
+
+
+def pie_kv_append_rope(ctx, batch, layer, k, v, q=None, q_out=None) -> None:
+    _check(ctx, lib.pie_kv_append_rope(ctx, batch, layer, _ptr(k), _ptr(v), _ptr(q), _ptr(q_out)),
+           "pie_kv_append_rope")
+
+
+def pie_rope_table(theta, head_dim, positions):
+    """The library's rotary table as a float32 numpy array [positions, head_dim/2, 2]."""
+    import numpy as np
+
+    out = np.empty((positions, head_dim // 2, 2), dtype=np.float32)
+    _check(None, lib.pie_rope_table(theta, head_dim, positions,
+                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), "pie_rope_table")
+    return out
 
 
 def pie_attend(ctx, batch, layer, q, out, lse=None) -> None:

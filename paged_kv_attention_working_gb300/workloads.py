@@ -68,6 +68,8 @@ class Workload:
     tok_streams: dict = field(default_factory=dict)    # name -> length
     page_size: int = 16
     logit_softcap: float = 0.0     # > 0: scores capped at c * tanh(s / c)
+    rope_theta: float = 0.0        # > 0: K (and Q) rotated by position before the append
+    rope_positions: int = 0        # positions the rotary table covers
     _cache: dict = field(default_factory=dict, repr=False)
 
     # --------------------------------------------------------------- inputs
@@ -322,15 +324,25 @@ FULL = {
 
 # Reduced-only variants: the same structure with e4m3 KV, and with a logit
 # soft cap of 3 (small enough that the cap bends N(0,1) scores visibly).
+# Variants with the rotary embedding fused into the append (Llama-3 base
+# 500000) take the same inputs rotated by position.
 EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_batch_e4m3_softcap",
-         "llama70b_fp8_softcap", "tiny_decode_softcap", "fork_spec_softcap")
+         "llama70b_fp8_softcap", "tiny_decode_softcap", "fork_spec_softcap",
+         "mixed_batch_rope", "llama70b_fp8_rope", "fork_spec_rope", "tiny_decode_rope")
 SOFTCAP_TEST = 3.0
+ROPE_THETA = 500000.0
 
 
 def reduced(name: str) -> Workload:
     """Oracle-sized variant of a full workload: same structure and head shapes,
     fewer working sets and shorter contexts, still several pages, splits and
     MMA tiles long with ragged tails."""
+    if name.endswith("_rope"):
+        w = reduced(name[: -len("_rope")])
+        w.name += "_rope"
+        w.rope_theta = ROPE_THETA
+        w.rope_positions = 16 * w.num_pages
+        return w
     if name.endswith("_softcap"):
         w = reduced(name[: -len("_softcap")])
         w.name += "_softcap"

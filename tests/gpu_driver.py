@@ -26,7 +26,8 @@ class GpuRun:
         self.ctx = pie.pie_ctx_create(w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages,
                                       kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(), k_scale=ks,
                                       v_scale=vs, k_pool=self.kpool, v_pool=self.vpool,
-                                      stream=self.stream.cuda_stream, logit_softcap=w.logit_softcap)
+                                      stream=self.stream.cuda_stream, logit_softcap=w.logit_softcap,
+                                      rope_theta=w.rope_theta, rope_max_positions=w.rope_positions)
         self.handles = {}
 
     def run(self, layers=None, kv_source=None):
@@ -63,7 +64,16 @@ class GpuRun:
                         kk, vv, qq = w.pass_inputs(segs, layer, want)
                         kd, vd = to_dev_bf16(kk), to_dev_bf16(vv)
                         qd = to_dev_bf16(qq) if want else None
-                    pie.pie_kv_append(self.ctx, b, layer, kd, vd)
+                    if w.rope_theta:
+                        # rotary embedding fused into the append; Q is rotated
+                        # into a new buffer that the attention then reads
+                        qr = torch.empty_like(qd) if want else None
+                        pie.pie_kv_append_rope(self.ctx, b, layer, kd, vd, qd if want else None, qr)
+                        if want:
+                            rec.setdefault("q_rot", {})[layer] = qr
+                            qd = qr
+                    else:
+                        pie.pie_kv_append(self.ctx, b, layer, kd, vd)
                     if want:
                         out = torch.empty((n, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
                         lse = torch.empty((n, w.num_q_heads), dtype=torch.float32, device="cuda")

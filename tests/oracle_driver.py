@@ -3,7 +3,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from oracle import attention, kvstore
+from oracle import attention, kvstore, rope
 
 
 def make_store(w, with_pool=True, page_size=None, free_list="seeded"):
@@ -44,8 +44,15 @@ def run(w, layers=None, with_pool=True, compute=True, store=None, on_pass=None, 
             pas = store.begin([(handles[s[0]], s[1], w.gather_tok(s[4])) for s in segs])
             rec = {"segs": segs, "pass": pas, "out": {}, "lse": {}}
             if with_pool:
+                if w.rope_theta:
+                    tab = rope.table(w.rope_theta, w.head_dim, max(pas.rows_pos, default=0) + 1)
                 for layer in (kv_layers if compute else ()):
                     k, v, q = w.pass_inputs(segs, layer, attend and layer in layers)
+                    if w.rope_theta and len(pas.rows_pos):
+                        k = rope.apply(k, pas.rows_pos, tab)
+                        if q is not None:
+                            q = rope.apply(q, pas.rows_pos, tab)
+                            rec.setdefault("q_rot", {})[layer] = q
                     store.kv_append(pas, layer, k, v)
                     if attend and layer in layers:
                         o, l = attention.attend_pass(store, pas, layer, kvstore.bf16_bits_to_f64(q),

@@ -50,6 +50,8 @@ def test_reduced_workload_parity(name):
     np.testing.assert_array_equal(vp, store.pool[1])
     assert len(passes) == len(ref_passes)
     for got, ref in zip(passes, ref_passes):
+        for layer, qr in got.get("q_rot", {}).items():   # rotated Q, bit for bit
+            np.testing.assert_array_equal(qr.view(torch.int16).cpu().numpy().view(np.uint16), ref["q_rot"][layer])
         for layer, out in got["out"].items():
             o = out.float().cpu().numpy()
             assert_close(o, ref["out"][layer], ATOL[w.kv_dtype], RTOL, f"{name} out layer {layer}")
@@ -125,3 +127,31 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     passes = g.run()                               # the full workload still runs and checks clean
     assert passes and pie.pie_ctx_check(g.ctx) == 0
     g.close()
+
+
+def test_rope_append_rejects_positions_past_the_table():
+    """A row at or past rope_max_positions is a range error with nothing
+    launched, and a context without a rotary table refuses the call."""
+    w = wl.tiny_decode()
+    g = gpu_driver.GpuRun(w)
+    pie.pie_ctx_destroy(g.ctx)
+    g.ctx = pie.pie_ctx_create(1, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages, k_pool=g.kpool,
+                               v_pool=g.vpool, stream=torch.cuda.current_stream().cuda_stream,
+                               rope_theta=10000.0, rope_max_positions=20)
+    h = pie.pie_ws_create(g.ctx)
+    b = pie.pie_batch_begin(g.ctx, [(h, 21, None)])
+    k = torch.zeros((21, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pie.PieError) as e:
+        pie.pie_kv_append_rope(g.ctx, b, 0, k, k)
+    assert e.value.status == pie.PIE_ERR_RANGE
+    pie.pie_batch_end(g.ctx, b)
+    assert not g.kpool.any()
+    g.close()
+    g2 = gpu_driver.GpuRun(w)
+    h = pie.pie_ws_create(g2.ctx)
+    b = pie.pie_batch_begin(g2.ctx, [(h, 1, None)])
+    with pytest.raises(pie.PieError) as e:
+        pie.pie_kv_append_rope(g2.ctx, b, 0, k, k)
+    assert e.value.status == pie.PIE_ERR_STATE
+    pie.pie_batch_end(g2.ctx, b)
+    g2.close()

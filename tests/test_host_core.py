@@ -265,6 +265,26 @@ def test_invalid_configurations_rejected():
     for cap in (-1.0, float("inf"), float("nan")):
         with pytest.raises(pie.PieError):
             pie.pie_ctx_create(1, 4, 2, 64, 8, logit_softcap=cap)       # soft cap must be finite, >= 0
+    for theta, npos in ((-1.0, 16), (1.0, 16), (float("inf"), 16), (float("nan"), 16), (10000.0, 0)):
+        with pytest.raises(pie.PieError):
+            pie.pie_ctx_create(1, 4, 2, 64, 8, rope_theta=theta, rope_max_positions=npos)
+
+
+@pytest.mark.parametrize("theta,d,positions", [(500000.0, 128, 33000), (10000.0, 64, 4096), (1234.5, 128, 2000)])
+def test_rope_table_matches_oracle_bit_for_bit(theta, d, positions):
+    from oracle import rope
+    np.testing.assert_array_equal(pie.pie_rope_table(theta, d, positions), rope.table(theta, d, positions))
+
+
+def test_rope_append_on_a_plan_only_context_is_a_state_error():
+    c = pie.pie_ctx_create(1, 4, 2, 64, 8, rope_theta=10000.0, rope_max_positions=20)
+    h = pie.pie_ws_create(c)
+    b = pie.pie_batch_begin(c, [(h, 21, None)])
+    with pytest.raises(pie.PieError) as e:
+        pie.pie_kv_append_rope(c, b, 0, 1, 1)
+    assert e.value.status == pie.PIE_ERR_STATE
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
 
 
 def test_plan_prefill_chunks_never_join_groups():
