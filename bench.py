@@ -258,7 +258,8 @@ def run_gpu(args, w, world, rank, local):
     ks, vs = w.scales()
     ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(),
                              k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream,
-                             logit_softcap=args.logit_softcap)
+                             logit_softcap=args.logit_softcap, rope_theta=args.rope_theta,
+                             rope_max_positions=(max(w.ctx) + 2) if args.rope_theta else 0)
     # set-up: every operation of the workload before its final (decode) pass,
     # with random bf16 K/V generated on the device
     gen = torch.Generator(device=dev)
@@ -302,6 +303,9 @@ def run_gpu(args, w, world, rank, local):
     kv_bytes_layer = keys * Hkv * D * esize * 2
     attend_bytes = kv_bytes_layer + 2 * n_rows * Hq * D * 2 + n_rows * Hq * 4 + 4 * pages
     append_bytes = n_rows * Hkv * D * (2 + esize) * 2
+    if args.rope_theta:
+        qr = torch.empty_like(q)
+        append_bytes += 2 * n_rows * Hq * D * 2 + n_rows * D * 4   # Q in and out, the rows' (cos, sin)
 
     info = {}
 
@@ -314,10 +318,13 @@ def run_gpu(args, w, world, rank, local):
         bb = pie.pie_batch_begin(ctx, segs)
         info.update(pie.pie_batch_plan_info(bb))
         for layer in range(L):
-            pie.pie_kv_append(ctx, bb, layer, kn[layer], vn[layer])
+            if args.rope_theta:
+                pie.pie_kv_append_rope(ctx, bb, layer, kn[layer], vn[layer], q[layer], qr[layer])
+            else:
+                pie.pie_kv_append(ctx, bb, layer, kn[layer], vn[layer])
             if ev is not None:
                 ev[layer][0].record(stream)
-            pie.pie_attend(ctx, bb, layer, q[layer], out[layer], lse[layer])
+            pie.pie_attend(ctx, bb, layer, qr[layer] if args.rope_theta else q[layer], out[layer], lse[layer])
             if ev is not None:
                 ev[layer][1].record(stream)
         pie.pie_batch_end(ctx, bb)
@@ -386,7 +393,7 @@ def run_gpu(args, w, world, rank, local):
                    "layers": L,
                    "hq": Hq, "hkv": Hkv, "head_dim": D, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
                    "page_size": 16, "l2": "inputs larger than L2 (~1.1 GB KV per layer)",
-                   "logit_softcap": args.logit_softcap,
+                   "logit_softcap": args.logit_softcap, "rope_theta": args.rope_theta,
                    "parallelism": f"replicas x{world}"},
         "rows_per_s": world * n_rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
@@ -523,6 +530,8 @@ def main():
                     help="working sets of the e4m3 workload (0 = the full 256; fewer only for profiling)")
     ap.add_argument("--logit-softcap", type=float, default=0.0,
                     help="logit soft cap c of the attention scores (0 = none)")
+    ap.add_argument("--rope-theta", type=float, default=0.0,
+                    help="rotary base: K and Q rotated in the append (pie_kv_append_rope); 0 = plain append")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
     args = ap.parse_args()
