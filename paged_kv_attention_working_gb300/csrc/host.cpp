@@ -240,7 +240,12 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
   }
   for (auto& s : segs)
     if (static_cast<int64_t>(s.n_new) * G <= kDecodeMaxM) dec_pages += s.n_pages - s.shared_pages;
-  int64_t target_items = std::max<int64_t>(1, static_cast<int64_t>(c->num_sms) * 8 / c->geo.hkv);
+  // KV splits aim at about 8 decode CTAs per SM for bf16 pages and 16 for
+  // e4m3 (measured on the 8B and 70B-FP8 decode batches: 1x and 2x were the
+  // best of 0.75x..3x; the e4m3 kernel spends more time per byte converting,
+  // and shorter splits keep its long tails off the end of the launch)
+  const int64_t per_sm = c->geo.kv_dtype == PIE_KV_E4M3 ? 16 : 8;
+  int64_t target_items = std::max<int64_t>(1, static_cast<int64_t>(c->num_sms) * per_sm / c->geo.hkv);
   int32_t chunk = static_cast<int32_t>(std::max<int64_t>(kMinSplitPages, (dec_pages + target_items - 1) / target_items));
 
   std::vector<int32_t> n_parts(n_rows, 0);
