@@ -328,7 +328,8 @@ FULL = {
 # 500000) take the same inputs rotated by position.
 EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_batch_e4m3_softcap",
          "llama70b_fp8_softcap", "tiny_decode_softcap", "fork_spec_softcap",
-         "mixed_batch_rope", "llama70b_fp8_rope", "fork_spec_rope", "tiny_decode_rope")
+         "mixed_batch_rope", "llama70b_fp8_rope", "fork_spec_rope", "tiny_decode_rope",
+         "mixed_batch_d64", "mixed_batch_d64_softcap", "mixed_batch_g8", "mixed_batch_e4m3_g8", "mixed_batch_mha")
 SOFTCAP_TEST = 3.0
 ROPE_THETA = 500000.0
 
@@ -364,6 +365,19 @@ def reduced(name: str) -> Workload:
     if name == "mixed_batch_e4m3":
         return mixed_batch(name="mixed_batch_e4m3_small", seed=17, n_chunks=3, chunk_lo=100, chunk_hi=300,
                            ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, kv_dtype=KV_E4M3)
+    # head shapes beyond the five workloads': d = 64 (both kernels), eight query
+    # heads per KV head on the tensor-core kernel, and one (plain multi-head)
+    if name == "mixed_batch_d64":
+        return mixed_batch(name="mixed_batch_d64_small", seed=19, n_chunks=3, chunk_lo=100, chunk_hi=300,
+                           ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, hq=8, hkv=2, d=64)
+    if name in ("mixed_batch_g8", "mixed_batch_e4m3_g8"):
+        e4 = name == "mixed_batch_e4m3_g8"
+        return mixed_batch(name=name + "_small", seed=20 + e4, n_chunks=3, chunk_lo=40, chunk_hi=120,
+                           ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, hq=64, hkv=8, d=128,
+                           kv_dtype=KV_E4M3 if e4 else KV_BF16)
+    if name == "mixed_batch_mha":
+        return mixed_batch(name="mixed_batch_mha_small", seed=22, n_chunks=3, chunk_lo=100, chunk_hi=300,
+                           ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, hq=8, hkv=8, d=128)
     if name == "llama70b_fp8":
         return decode_batch(name="llama70b_fp8_small", seed=15, n_ws=8, ctx_lo=300, ctx_hi=1200,
                             num_layers=1, hq=64, hkv=8, d=128, kv_dtype=KV_E4M3,
