@@ -7,11 +7,14 @@
 // heads of that KV group (M, in two 128-row tiles t = 0, 1), which all read
 // the same run of pages, causally (key position <= row position).  Keys go
 // in tiles of 128 (8 pages):
-//   producer warp   bulk copies of 2-KB page panels into a K ring and a V
-//                   ring (separate, so a K tile is refilled as soon as both
-//                   S products have read it); the pool's block layout is the
-//                   128-byte-swizzled operand layout, so pages land ready for
-//                   the tensor cores (K-major for K, MN-major for V);
+//   producer warps  one for K, one for V (each issue of a bulk copy costs
+//                   about a hundred cycles, so one warp for both lagged):
+//                   2-KB page panels into a K ring, whole page blocks into a
+//                   V ring (separate rings, so a K tile is refilled as soon
+//                   as both S products have read it); the pool's block
+//                   layout is the 128-byte-swizzled operand layout, so pages
+//                   land ready for the tensor cores (K-major for K, MN-major
+//                   for V, one page per K = 16 step);
 //   MMA thread      event-driven issue of S_t = Q_t K^T (tcgen05.mma M=128
 //                   N=128 K=16, fp32 in tensor memory) and O_t += P_t V
 //                   (M=128 N=d K=16, A = P read from tensor memory, O in
@@ -52,11 +55,11 @@
 namespace pie {
 namespace {
 
-// Warps 0-7 softmax, warp 8 MMA, warp 9 producer; e4m3 adds converter
-// warps 10 and 11.
+// Warps 0-7 softmax, warp 8 MMA; bf16: warp 9 produces K and warp 10 V;
+// e4m3: warp 9 produces raw K and V, warps 10 and 11 convert them.
 template <int D, bool E4M3>
 struct PreCfg {
-  static constexpr int kThreads = E4M3 ? 384 : 320;
+  static constexpr int kThreads = E4M3 ? 384 : 352;
   static constexpr int kPanels = D / 64;
   static constexpr int kKeys = 128;                       // keys per tile
   static constexpr int kPagesPerTile = kKeys / kPageSize;  // 8
@@ -303,60 +306,54 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
         mbar_arrive(is_v ? &v_full[st] : &k_full[st]);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ producer
-    // K(j) and V(j) each take one copy per lane: 8 pages x kPanels panels.
+  } else if (warp == 9 || warp == 10) {
+    // ----------------------------------------------------------- producers
+    // warp 9: K(j), one 2-KB copy per page panel (8 pages x kPanels) into
+    // the panel-major tile (the S product's K-major operand spans pages);
+    // warp 10: V(j), one copy of each whole page block (8 pages), blocks
+    // side by side (the PV product takes one page per K = 16 step, its two
+    // panels block_bytes / 2 apart).  In tile order, a stage once the MMAs
+    // that read it are done; the page ids are loaded a tile ahead.
+    const bool is_v = warp == 10;
+    const int nst = is_v ? C::kVStages : C::kKStages;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    const int ncopy = is_v ? C::kPagesPerTile : C::kPagesPerTile * C::kPanels;
     const int64_t layer_blk = static_cast<int64_t>(layer) * g.num_pages * g.hkv;
-    constexpr int kCopies = C::kPagesPerTile * C::kPanels;
-    int kn = 0, vn = 0;
-    uint32_t idle = 0;
-    while ((kn < nkv || vn < nkv) && idle < kWaitLimit) {
-      int which = -1;  // lane 0 decides: 0 = K(kn), 1 = V(vn)
-      if (lane == 0) {
-        if (kn < nkv && (kn < C::kKStages ||
-                         mbar_test_wait(&k_empty[kn % C::kKStages], ((kn / C::kKStages) - 1) & 1)))
-          which = 0;
-        else if (vn < kn && (vn < C::kVStages ||
-                             mbar_test_wait(&v_empty[vn % C::kVStages], ((vn / C::kVStages) - 1) & 1)))
-          which = 1;
-        if (which == 0) mbar_arrive_expect_tx(&k_full[kn % C::kKStages], C::kKVTile);
-        if (which == 1) mbar_arrive_expect_tx(&v_full[vn % C::kVStages], C::kKVTile);
-      }
-      which = __shfl_sync(0xffffffffu, which, 0);
-      if (which < 0) {
-        ++idle;
-        continue;
-      }
-      idle = 0;
-      const int j = which == 0 ? kn : vn;
-      if (lane < kCopies) {
-        const int pg = lane / C::kPanels, panel = lane % C::kPanels;
-        int pj = C::kPagesPerTile * j + pg;
-        if (pj >= it.n_pages) pj = it.n_pages - 1;  // keys there are masked; any finite page will do
-        const int page = p.page_ids[it.pages_off + pj];
-        const int64_t off = (layer_blk + static_cast<int64_t>(page) * g.hkv + head) * g.block_bytes + panel * 2048;
-        if (which == 0) {
-          uint8_t* dst = smem + C::kOffK + (j % C::kKStages) * C::kKVTile + panel * C::kPanelBytes + pg * 2048;
-          bulk_g2s(dst, kpool + off, 2048, &k_full[j % C::kKStages]);
+    auto page_of = [&](int j) {
+      int pj = C::kPagesPerTile * j + (is_v ? lane : lane / C::kPanels);
+      if (pj >= it.n_pages) pj = it.n_pages - 1;  // keys there are masked; any finite page will do
+      return lane < ncopy ? p.page_ids[it.pages_off + pj] : 0;
+    };
+    int page = nkv > 0 ? page_of(0) : 0;
+    bool ok = true;
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int st = j % nst;
+      if (j >= nst) ok = warp_wait(&empty[st], ((j / nst) - 1) & 1, err);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], C::kKVTile);
+      __syncwarp();
+      if (lane < ncopy) {
+        const int64_t blk = (layer_blk + static_cast<int64_t>(page) * g.hkv + head) * g.block_bytes;
+        if (is_v) {
+          bulk_g2s(smem + C::kOffV + st * C::kKVTile + lane * g.block_bytes, vpool + blk,
+                   static_cast<uint32_t>(g.block_bytes), &full[st]);
         } else {
-          uint8_t* dst = smem + C::kOffV + (j % C::kVStages) * C::kKVTile + panel * C::kPanelBytes + pg * 2048;
-          bulk_g2s(dst, vpool + off, 2048, &v_full[j % C::kVStages]);
+          const int pg = lane / C::kPanels, panel = lane % C::kPanels;
+          bulk_g2s(smem + C::kOffK + st * C::kKVTile + panel * C::kPanelBytes + pg * 2048, kpool + blk + panel * 2048,
+                   2048, &full[st]);
         }
       }
-      if (which == 0)
-        ++kn;
-      else
-        ++vn;
+      if (j + 1 < nkv) page = page_of(j + 1);
       __syncwarp();
     }
-    if (idle >= kWaitLimit && lane == 0 && err) atomicOr(err, kErrWaitTimeout);
   } else if (warp == 8) {
     // ----------------------------------------------------------------- MMA
     // One thread issues everything, event-driven, PVs first (they gate the
     // next S of their tile): PV_t(j) once P_t(j) is written and V(j)
     // landed; S_t(j) once K(j) landed and PV_t(j-1) is complete (S_t(j)
     // overwrites P_t(j-1)).  A K (V) stage is released by a commit after the
-    // last S (PV) that reads it.
+    // last S (PV) that reads it.  (Issuing S first measured the same.)
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16kind(128, C::kKeys, false, false, !E4M3);
       const uint32_t id_o = tc::idesc_f16kind(128, D, false, true, !E4M3);
@@ -375,8 +372,10 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
             const uint32_t d_o = tmem + C::kColO + t * D;
 #pragma unroll
             for (int ks = 0; ks < C::kKeys / 16; ++ks)
-              tc::mma_bf16_ts(d_o, p_tmem + ks * 8, tc::sw128_desc(vaddr + ks * 2048, C::kPanelBytes, 1024), id_o,
-                              j > 0 || ks > 0);
+              tc::mma_bf16_ts(d_o, p_tmem + ks * 8,
+                              E4M3 ? tc::sw128_desc(vaddr + ks * 2048, C::kPanelBytes, 1024)
+                                   : tc::sw128_desc(vaddr + ks * (16 * D * 2), 2048, 1024),
+                              id_o, j > 0 || ks > 0);
             tc::commit(&o_done[t]);
             pv_next[t] = j + 1;
             if (pv_next[1 - t] > j) tc::commit(&v_empty[j % C::kVStages]);
