@@ -13,7 +13,7 @@ def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
     return t.to("cuda").view(torch.bfloat16)
 
 
-class GpuRun:
+class DeviceRun:
     def __init__(self, w, device="cuda"):
         self.w = w
         esize = 2 if w.kv_dtype == pie.PIE_KV_BF16 else 1

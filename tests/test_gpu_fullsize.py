@@ -107,7 +107,7 @@ def check(w, names, layers, rows_of=None):
     oracle; compares pool bytes and attention rows of the named sets."""
     sub = sub_workload(w, names)
     store, ohandles, ref_passes = oracle_driver.run(sub, layers=layers, kv_layers=layers)
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     passes = g.run(layers=layers, kv_source=exact_source(w, set(names)))
     # appended bytes, page by page in logical order, valid slots only
     esize = 2 if w.kv_dtype == wl.KV_BF16 else 1

@@ -43,7 +43,7 @@ def _cuda():
 def test_reduced_workload_parity(name):
     w = wl.reduced(name)
     store, handles, ref_passes = oracle_driver.run(w)
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     passes = g.run()
     kp, vp = g.pools()
     np.testing.assert_array_equal(kp, store.pool[0])
@@ -70,7 +70,7 @@ def test_e4m3_append_matches_codec_over_all_bf16(scale):
     k[: bits.size] = bits
     k = k.reshape(n, 1, 128)
     w = wl.Workload("e4m3_all", 0, 1, 1, 1, 128, wl.KV_E4M3, -(-n // 16) + 1, [])
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     pie.pie_ctx_destroy(g.ctx)
     g.ctx = pie.pie_ctx_create(1, 1, 1, 128, w.num_pages, kv_dtype=pie.PIE_KV_E4M3, k_scale=[scale],
                                v_scale=[scale], k_pool=g.kpool, v_pool=g.vpool,
@@ -92,7 +92,7 @@ def test_e4m3_append_matches_codec_over_all_bf16(scale):
 
 def test_pool_exhaustion_leaves_state_and_device_unchanged():
     w = wl.tiny_decode()
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     h = pie.pie_ws_create(g.ctx)
     with pytest.raises(pie.PieError) as e:
         pie.pie_batch_begin(g.ctx, [(h, 16 * (w.num_pages + 1), None)])
@@ -104,7 +104,7 @@ def test_pool_exhaustion_leaves_state_and_device_unchanged():
 
 def test_empty_batch_is_a_no_op():
     w = wl.tiny_decode()
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     h = pie.pie_ws_create(g.ctx)
     b = pie.pie_batch_begin(g.ctx, [(h, 0, None)])
     assert pie.pie_batch_rows(b) == 0
@@ -119,7 +119,7 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     """A kernel wait that can never complete ends after its poll limit, sets
     the error bit the host reads, and leaves the context usable."""
     w = wl.tiny_decode()
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     assert pie.pie_ctx_check(g.ctx) == 0
     pie.pie_selftest_wait_timeout(g.ctx, 1000)
     assert pie.pie_ctx_check(g.ctx) == 1
@@ -133,7 +133,7 @@ def test_rope_append_rejects_positions_past_the_table():
     """A row at or past rope_max_positions is a range error with nothing
     launched, and a context without a rotary table refuses the call."""
     w = wl.tiny_decode()
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     pie.pie_ctx_destroy(g.ctx)
     g.ctx = pie.pie_ctx_create(1, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_pages, k_pool=g.kpool,
                                v_pool=g.vpool, stream=torch.cuda.current_stream().cuda_stream,
@@ -147,7 +147,7 @@ def test_rope_append_rejects_positions_past_the_table():
     pie.pie_batch_end(g.ctx, b)
     assert not g.kpool.any()
     g.close()
-    g2 = gpu_driver.GpuRun(w)
+    g2 = gpu_driver.DeviceRun(w)
     h = pie.pie_ws_create(g2.ctx)
     b = pie.pie_batch_begin(g2.ctx, [(h, 1, None)])
     with pytest.raises(pie.PieError) as e:

@@ -40,7 +40,7 @@ def _close(got, ref, what):
 ])
 def test_noalloc_decode_matches_attend_on_two_calls(name, kw):
     w = wl.decode_batch(**kw)
-    g = gpu_driver.GpuRun(w)
+    g = gpu_driver.DeviceRun(w)
     passes = g.run()
     dec = passes[-1]
     segs = dec["segs"]
