@@ -310,10 +310,10 @@ def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=
     return w
 
 
-# The five workloads at full size (the parity tests also run reduced-size
-# variants of 2-5 that the oracle finishes in seconds, and e4m3-KV variants
-# of the fork and mixed workloads, which take the tensor-core path with
-# e4m3 pages).
+# The five workloads at full size.  The parity tests also run oracle-sized
+# reductions of the decode, fork, mixed and 70B-shaped ones (see reduced),
+# plus variants with e4m3 KV, a logit soft cap, the fused rotary embedding
+# and other head shapes.
 FULL = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
