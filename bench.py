@@ -411,6 +411,99 @@ def run_gpu(args, w, world, rank, local):
     return result
 
 
+def run_fork(args, world, rank, local):
+    """Fork / speculative decoding: a 4096-token prompt forked into 10 working
+    sets, each with its own frozen suffix, then one pass of 4 draft tokens per
+    fork (40 query rows, causal among each fork's drafts), every layer, rolled
+    back after each step.  The shared prompt pages are read once per pass; the
+    line also reports what the same reads would cost if every fork read the
+    prompt itself."""
+    import torch
+
+    from paged_kv_attention_working_gb300 import pie
+    from paged_kv_attention_working_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    L = args.layers
+    w = wl.fork_spec(num_layers=L, unshared=False)
+    Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+    pool_bytes = L * w.num_pages * Hkv * 16 * D * 2
+    kpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+    vpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+    ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, free_list=w.free_list().tolist(), k_pool=kpool,
+                             v_pool=vpool, stream=stream.cuda_stream, logit_softcap=args.logit_softcap)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000 + rank)
+    hs = {}
+    first_attend = min(i for i, op in enumerate(w.ops) if op[0] == "pass" and op[2])
+    for op in w.ops[:first_attend]:
+        if op[0] == "create":
+            hs[op[1]] = pie.pie_ws_create(ctx)
+        elif op[0] == "fork":
+            hs[op[2]] = pie.pie_ws_fork(ctx, hs[op[1]])
+        elif op[0] == "freeze":
+            pie.pie_ws_freeze(ctx, hs[op[1]], op[2])
+        elif op[0] == "pass":
+            b = pie.pie_batch_begin(ctx, [(hs[sg[0]], sg[1], None) for sg in op[1]])
+            n = pie.pie_batch_rows(b)
+            for layer in range(L):
+                k = torch.randn((n, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+                pie.pie_kv_append(ctx, b, layer, k, k)
+            pie.pie_batch_end(ctx, b)
+    segs = [(hs[sg[0]], sg[1], None) for sg in w.ops[first_attend][1]]
+    drafts = segs[0][1]
+    rows = sum(sg[1] for sg in segs)
+    q = torch.randn((L, rows, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
+    kv = torch.randn((L, rows, Hkv, D), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty((L, rows, Hq, D), dtype=torch.bfloat16, device=dev)
+    prompt = w.kv_streams["prompt"]
+    # keys read per layer: the shared prompt once, each fork's suffix and
+    # drafts (every draft row sees the drafts before it; the bytes count each
+    # key once per fork)
+    private = sum(s + drafts for s in w.suffix)
+    kv_bytes_layer = (prompt + private) * Hkv * D * 2 * 2
+    unshared_layer = (len(segs) * prompt + private) * Hkv * D * 2 * 2
+
+    def step():
+        bb = pie.pie_batch_begin(ctx, segs)
+        for layer in range(L):
+            pie.pie_kv_append(ctx, bb, layer, kv[layer], kv[layer])
+            pie.pie_attend(ctx, bb, layer, q[layer], out[layer])
+        pie.pie_batch_end(ctx, bb)
+        for sg in segs:
+            pie.pie_ws_rollback(ctx, sg[0], drafts)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = allmax(world, t0.elapsed_time(t1) / args.steps)
+    assert pie.pie_ctx_check(ctx) == 0
+    hbm, src = peaks()
+    value = world * kv_bytes_layer * L / (ms * 1e-3) / 1e9
+    res = {"metric": "fork decode attend KV GB/s (shared prompt read once per pass)", "value": value, "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": "fork_spec", "prompt": prompt, "forks": len(segs), "drafts": drafts,
+                      "suffix_tokens": w.suffix, "layers": L, "hq": Hq, "hkv": Hkv, "head_dim": D,
+                      "l2": "32 layers of K/V (about 0.7 GB per step), larger than L2"},
+           "rows_per_s": world * rows / (ms * 1e-3),
+           "unshared_equivalent_GBps": world * unshared_layer * L / (ms * 1e-3) / 1e9,
+           "roofline": {"bound": "hbm", "kernel": "whole fork pass (append, tensor-core shared prefix, decode suffixes, merge)",
+                        "achieved": value, "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": value / hbm,
+                        "traffic": None}}
+    pie.pie_ctx_destroy(ctx)
+    return res
+
+
 def run_mixed(args, w, world, rank, local):
     """Mixed continuous batch (16 prefill chunks + 128 decode rows, one
     pie_attend): times the whole step, and the chunks alone (the tensor-core
@@ -525,7 +618,7 @@ def main():
                     help="CPU seconds of oracle work (whole reference run, or the cpu_baseline sample)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "mixed_batch", "mixed_batch_e4m3", "llama70b_fp8"])
+                    choices=["llama8b_decode", "mixed_batch", "mixed_batch_e4m3", "llama70b_fp8", "fork_spec"])
     ap.add_argument("--n-ws", type=int, default=0,
                     help="working sets of the e4m3 workload (0 = the full 256; fewer only for profiling)")
     ap.add_argument("--logit-softcap", type=float, default=0.0,
@@ -538,6 +631,16 @@ def main():
     from paged_kv_attention_working_gb300 import workloads as wl
 
     world, rank, local = dist_init()
+    if args.workload == "fork_spec":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the decode workloads; "
+                                  "the fork pass is timed on the GPU only"}), flush=True)
+            return
+        res = run_fork(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     if args.workload.startswith("mixed_batch"):
         if args.impl == "reference":
             if rank == 0:
