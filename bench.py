@@ -60,14 +60,37 @@ def traffic(key, files, algorithmic):
     return rec["dram_bytes_per_launch"] * algorithmic / rec["algorithmic_per_launch"]
 
 
-def peaks():
+def _measured(keys):
+    """A number from MEASURED_PEAKS.json (first of keys present; a nested
+    {"value": ...} is unwrapped), or None."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
+    if not os.path.exists(path):
+        return None
+    try:
         with open(path) as f:
             d = json.load(f)
-        hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
-        return float(hbm), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+    except (OSError, ValueError):
+        return None
+    for k in keys:
+        v = d.get(k)
+        if isinstance(v, dict):
+            v = v.get("value")
+        if isinstance(v, (int, float)) and v > 0:
+            return float(v)
+    return None
+
+
+def peaks():
+    """HBM copy bandwidth (GB/s) for the roofline, measured when available."""
+    hbm = _measured(("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"))
+    return (hbm, "measured") if hbm else (FALLBACK_HBM_GBS, "fallback")
+
+
+def tensor_peak():
+    """Dense bf16 tensor throughput (TFLOP/s), the burst figure (a prefill
+    launch is timed on its own), measured when available."""
+    t = _measured(("bf16_tflops", "bf16_TFLOPs"))
+    return (t, "measured") if t else (FALLBACK_BF16_TFLOPS, "fallback")
 
 
 class Clocks:
@@ -579,14 +602,7 @@ def run_mixed(args, w, world, rank, local):
     t_chunks = timed(chunk_segs, make(chunk_segs), args.steps)
     t_mixed = timed(main_segs, make(main_segs), args.steps)
     tflops = flops / (t_chunks * 1e-3) / 1e12
-    peak = FALLBACK_BF16_TFLOPS
-    src = "fallback"
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
-        with open(path) as f:
-            d = json.load(f)
-        if d.get("bf16_tflops"):
-            peak, src = float(d["bf16_tflops"]), "measured"
+    peak, src = tensor_peak()
     res = {"metric": "prefill attend TFLOP/s (causal-exact flops)", "value": tflops, "unit": "TFLOP/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mixed,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
