@@ -91,7 +91,12 @@ typedef struct pie_config {
                             v_pool = plan-only context (host state only, no
                             device work; pie_kv_append / pie_attend fail) */
   void* v_pool;
-  void* stream;          /* cudaStream_t, borrowed; NULL = legacy default */
+  void* stream;          /* cudaStream_t, borrowed; NULL = legacy default.
+                            The context also creates one non-blocking stream
+                            of its own: in a pass with both decode-kernel and
+                            tensor-core items, pie_attend runs the decode
+                            launch there, forked from and joined back into
+                            `stream` by events within the call */
   float logit_softcap;   /* ops.attn.logit_softcap ("Poem ops"): c > 0 replaces
                             every scaled score s by c * tanh(s / c) before the
                             softmax (the LSE is over the capped scores);

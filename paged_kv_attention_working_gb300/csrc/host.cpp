@@ -97,6 +97,10 @@ struct pie_ctx {
   uint8_t* h_plan = nullptr;  // pinned staging
   size_t h_plan_cap = 0;
   cudaEvent_t upload_done = nullptr;
+  // a second stream, so a pass's decode items run beside its tensor-core
+  // items (fork: side waits on main; join: main waits on side)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   bool upload_pending = false;
   float* d_part = nullptr;  // partial (acc | m,l) results
   size_t part_cap = 0;      // floats
@@ -451,6 +455,9 @@ pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&c->d_err), sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->fork_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join_ev, cudaEventDisableTiming);
     if (e == cudaSuccess && k.rope_theta > 0.0f) {
       std::vector<float> tab(static_cast<size_t>(k.rope_max_positions) * k.head_dim);
       pie_rope_table(k.rope_theta, k.head_dim, k.rope_max_positions, tab.data());
@@ -477,6 +484,12 @@ pie_status pie_ctx_destroy(pie_ctx* c) {
     if (c->d_part) cudaFree(c->d_part);
     if (c->h_plan) cudaFreeHost(c->h_plan);
     if (c->upload_done) cudaEventDestroy(c->upload_done);
+    if (c->side) {
+      cudaStreamSynchronize(c->side);
+      cudaStreamDestroy(c->side);
+    }
+    if (c->fork_ev) cudaEventDestroy(c->fork_ev);
+    if (c->join_ev) cudaEventDestroy(c->join_ev);
   }
   delete c->open;
   delete c;
@@ -830,12 +843,23 @@ pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, vo
   size_t total_parts = c->part_cap / (static_cast<size_t>(c->geo.hq) * (c->geo.d + 2));
   float* ml = c->d_part + total_parts * c->geo.hq * c->geo.d;
   cudaError_t e = cudaSuccess;
-  if (v.n_pre)
-    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
-                            lse, acc, ml, c->d_err, c->stream);
+  // With both kinds of items, the decode launch goes on the side stream so
+  // it can take the SMs the tensor-core launch leaves free (a small pass
+  // fills only part of the GPU); the two write disjoint outputs and
+  // partials, and the merge waits for both.
+  const bool both = v.n_pre && v.n_dec;
+  if (both) {
+    e = cudaEventRecord(c->fork_ev, c->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->side, c->fork_ev, 0);
+  }
   if (e == cudaSuccess && v.n_dec)
     e = pie::launch_decode(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
-                           lse, acc, ml, c->d_err, c->stream);
+                           lse, acc, ml, c->d_err, both ? c->side : c->stream);
+  if (e == cudaSuccess && both) e = cudaEventRecord(c->join_ev, c->side);
+  if (e == cudaSuccess && v.n_pre)
+    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
+                            lse, acc, ml, c->d_err, c->stream);
+  if (e == cudaSuccess && both) e = cudaStreamWaitEvent(c->stream, c->join_ev, 0);
   if (e == cudaSuccess && v.n_merge) e = pie::launch_merge(c->geo, v, out, lse, acc, ml, c->stream);
   if (e != cudaSuccess) return cuda_fail(c, e, "attend launch");
   return PIE_OK;
