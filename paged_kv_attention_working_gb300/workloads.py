@@ -310,6 +310,46 @@ def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=
     return w
 
 
+def edge_batch(name="edge_batch", seed=30, kv_dtype=KV_BF16, hq=32, hkv=8, d=128,
+               chunks=((1, 0), (16, 0), (17, 15), (255, 1), (256, 16), (257, 4095), (128, 128), (2, 4094)),
+               decodes=(0, 1, 15, 16, 17, 127, 128, 129), idle_ctx=40) -> Workload:
+    """One pass of ragged edges: prefill chunks of (new tokens, context) at
+    page (16) and row-tile boundaries, single-token rows on contexts around
+    page and key-tile (128) boundaries -- context 0 sees only its own key --
+    and a working set in the pass with no new tokens."""
+    ops = []
+    w = Workload(name, seed, 1, hq, hkv, d, kv_dtype, 0, ops)
+    fill, main = [], []
+    lengths = []
+    for i, (n, c) in enumerate(chunks):
+        ops.append(("create", f"c{i}"))
+        w.kv_streams[f"cctx{i}"] = c + n
+        w.q_streams[f"cq{i}"] = n
+        if c:
+            fill.append((f"c{i}", c, [(f"cctx{i}", 0, c)], None, None))
+        main.append((f"c{i}", n, [(f"cctx{i}", c, n)], [(f"cq{i}", 0, n)], None))
+        lengths.append(c + n)
+    for i, c in enumerate(decodes):
+        ops.append(("create", f"d{i}"))
+        w.kv_streams[f"dctx{i}"] = c + 1
+        w.q_streams[f"dq{i}"] = 1
+        if c:
+            fill.append((f"d{i}", c, [(f"dctx{i}", 0, c)], None, None))
+        main.append((f"d{i}", 1, [(f"dctx{i}", c, 1)], [(f"dq{i}", 0, 1)], None))
+        lengths.append(c + 1)
+    ops.append(("create", "idle"))
+    w.kv_streams["idle"] = idle_ctx
+    fill.append(("idle", idle_ctx, [("idle", 0, idle_ctx)], None, None))
+    main.append(("idle", 0, [], [], None))
+    lengths.append(idle_ctx)
+    ops.append(("pass", fill, False))
+    ops += [("freeze", f"c{i}", -1) for i in range(len(chunks))]
+    ops += [("freeze", f"d{i}", -1) for i in range(len(decodes))]
+    ops.append(("pass", main, True))
+    w.num_pages = _pages_for(lengths) + 16
+    return w
+
+
 # The five workloads at full size.  The parity tests also run oracle-sized
 # reductions of the decode, fork, mixed and 70B-shaped ones (see reduced),
 # plus variants with e4m3 KV, a logit soft cap, the fused rotary embedding
@@ -329,7 +369,8 @@ FULL = {
 EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_batch_e4m3_softcap",
          "llama70b_fp8_softcap", "tiny_decode_softcap", "fork_spec_softcap",
          "mixed_batch_rope", "llama70b_fp8_rope", "fork_spec_rope", "tiny_decode_rope",
-         "mixed_batch_d64", "mixed_batch_d64_softcap", "mixed_batch_g8", "mixed_batch_e4m3_g8", "mixed_batch_mha")
+         "mixed_batch_d64", "mixed_batch_d64_softcap", "mixed_batch_g8", "mixed_batch_e4m3_g8", "mixed_batch_mha",
+         "edge_batch", "edge_batch_e4m3")
 SOFTCAP_TEST = 3.0
 ROPE_THETA = 500000.0
 
@@ -378,6 +419,10 @@ def reduced(name: str) -> Workload:
     if name == "mixed_batch_mha":
         return mixed_batch(name="mixed_batch_mha_small", seed=22, n_chunks=3, chunk_lo=100, chunk_hi=300,
                            ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, hq=8, hkv=8, d=128)
+    if name == "edge_batch":
+        return edge_batch()
+    if name == "edge_batch_e4m3":
+        return edge_batch(name="edge_batch_e4m3", seed=31, kv_dtype=KV_E4M3)
     if name == "llama70b_fp8":
         return decode_batch(name="llama70b_fp8_small", seed=15, n_ws=8, ctx_lo=300, ctx_hi=1200,
                             num_layers=1, hq=64, hkv=8, d=128, kv_dtype=KV_E4M3,
