@@ -53,6 +53,7 @@ def sub_workload(w, names):
             ops.append(op)
     sub = wl.Workload(w.name + "_sub", w.seed, w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim,
                       w.kv_dtype, 0, ops, dict(w.kv_streams), dict(w.q_streams), dict(w.tok_streams))
+    sub.logit_softcap, sub.rope_theta, sub.rope_positions = w.logit_softcap, w.rope_theta, w.rope_positions
     # pages needed: replay on a page-count-only store and keep the peak
     big = 1 << 20
     st = kvstore.KVStore(w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim, big, with_pool=False)
@@ -179,4 +180,28 @@ def test_mixed_batch_full(kv_dtype):
 def test_llama70b_fp8_full():
     w = wl.llama70b_fp8()
     names = [f"w{i}" for i in range(248, 256)]  # the last dedup group (prefix writer + 7 matches)
+    check(w, names, layers=[0])
+
+
+def test_mixed_batch_full_softcap():
+    w = wl.mixed_batch()
+    w.logit_softcap = 5.0
+    chunks = list(np.argsort(w.chunks))
+    names = [f"c{chunks[-1]}", "d5"]
+    rng = np.random.default_rng(1)
+
+    def rows_of(n, count):
+        if count <= 64:
+            return slice(None)
+        return np.unique(np.concatenate([np.arange(8), np.arange(count - 8, count), rng.integers(0, count, 48)]))
+
+    check(w, names, layers=[0], rows_of=rows_of)
+
+
+def test_llama8b_decode_full_rope():
+    w = wl.llama8b_decode()
+    w.rope_theta = 500000.0
+    w.rope_positions = max(w.ctx) + 2
+    order = np.argsort(w.ctx)
+    names = [f"w{order[0]}", f"w{order[-1]}"]
     check(w, names, layers=[0])
