@@ -22,7 +22,9 @@
  *    stream-ordered use on the context's stream; no call synchronises that
  *    stream except where stated (pie_ctx_destroy, buffer growth in
  *    pie_batch_begin).
- *  - All device work of a context runs on its stream, in call order.  The
+ *  - All device work of a context is ordered on its stream, in call order
+ *    (pie_attend may run part of a pass on a second stream the context owns,
+ *    forked from and joined back into that stream within the call).  The
  *    caller must keep pools, inputs and outputs alive until that work ends.
  *
  * KV pool layout (device memory owned by the caller, borrowed by the
