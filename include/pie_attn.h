@@ -120,10 +120,12 @@ typedef struct pie_seg {
   const int32_t* token_ids;
 } pie_seg;
 
-/* Context.  Copies the configuration, allocates small device buffers
- * (scales, plan, partial results) with cudaMalloc when k_pool is set. */
+/* Context.  Copies the configuration; when k_pool is set, allocates its
+ * device buffers (scales, the rotary table when rope_theta > 0, the plan,
+ * partial results) with cudaMalloc and creates a second stream and two
+ * events of its own. */
 pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out);
-/* Synchronises the stream, frees everything the context allocated. */
+/* Synchronises the streams, frees everything the context allocated. */
 pie_status pie_ctx_destroy(pie_ctx* ctx);
 const char* pie_last_error(const pie_ctx* ctx);
 
