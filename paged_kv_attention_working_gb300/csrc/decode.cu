@@ -260,23 +260,24 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
         mma16816<true>(o[2 * np + 1], pa, b2, b3);
       }
     } else {
+      // Transposing loads of 16-bit units (two e4m3 dims): matrices (keys
+      // 0-7, chunk 2cp), (keys 8-15, 2cp), (0-7, 2cp+1), (8-15, 2cp+1); each
+      // register holds (key 2t: dims 2g, 2g+1) (key 2t+1: dims 2g, 2g+1),
+      // and one byte permute pairs the keys per dim.  n-tile 2c takes dims
+      // 16c + 2n, n-tile 2c+1 dims 16c + 2n + 1 (undone when writing out).
+      const int vkey = (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int vsel = lane >> 4;
 #pragma unroll
-      for (int mq = 0; mq < D / 32; ++mq) {
-        uint32_t w[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          int key = 2 * tq + (jj & 1) + ((jj >> 1) << 3);
-          int c = 2 * mq + (gq >> 2);
-          w[jj] = lds32(vb + key * 128 + 16 * (c ^ (key & 7)) + 4 * (gq & 3));
-        }
-#pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-          // bytes: (key 2t, d_i) (key 2t+1, d_i) (key 2t, d_i+1) (key 2t+1, d_i+1), same for keys 2t+8, 2t+9
-          const uint32_t sel = i | ((4 + i) << 4) | ((i + 1) << 8) | ((5 + i) << 12);
-          const uint32_t x01 = prmt(w[0], w[1], sel), x23 = prmt(w[2], w[3], sel);
-          mma16816<false>(o[4 * mq + i], pa, e4m3x2_lo_to_f16x2(x01), e4m3x2_lo_to_f16x2(x23));
-          mma16816<false>(o[4 * mq + i + 1], pa, e4m3x2_hi_to_f16x2(x01), e4m3x2_hi_to_f16x2(x23));
-        }
+      for (int cp = 0; cp < D / 32; ++cp) {
+        const int c = 2 * cp + vsel;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vb + vkey * 128 + 16 * (c ^ (vkey & 7)), r0, r1, r2, r3);
+        const uint32_t x0 = prmt(r0, r0, 0x3120), x1 = prmt(r1, r1, 0x3120);
+        const uint32_t x2 = prmt(r2, r2, 0x3120), x3 = prmt(r3, r3, 0x3120);
+        mma16816<false>(o[4 * cp], pa, e4m3x2_lo_to_f16x2(x0), e4m3x2_lo_to_f16x2(x1));
+        mma16816<false>(o[4 * cp + 1], pa, e4m3x2_hi_to_f16x2(x0), e4m3x2_hi_to_f16x2(x1));
+        mma16816<false>(o[4 * cp + 2], pa, e4m3x2_lo_to_f16x2(x2), e4m3x2_lo_to_f16x2(x3));
+        mma16816<false>(o[4 * cp + 3], pa, e4m3x2_hi_to_f16x2(x2), e4m3x2_hi_to_f16x2(x3));
       }
     }
     __syncwarp();
@@ -341,10 +342,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
         if constexpr (!E4M3) {
           *reinterpret_cast<uint32_t*>(dst + 8 * i + 2 * tq) =
               pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
-        } else {
-          int mq = i >> 2, ii = i & 3;
-          dst[32 * mq + 8 * tq + ii] = __float2bfloat16_rn(o[i][2 * h] * inv);
-          dst[32 * mq + 8 * tq + 4 + ii] = __float2bfloat16_rn(o[i][2 * h + 1] * inv);
+        } else if ((i & 1) == 0) {
+          // n-tiles i (even dims) and i+1 (odd dims) of chunk i/2: dims
+          // 8i + 4t .. 8i + 4t + 3
+          uint2 wv;
+          wv.x = pack_bf16(o[i][2 * h] * inv, o[i + 1][2 * h] * inv);
+          wv.y = pack_bf16(o[i][2 * h + 1] * inv, o[i + 1][2 * h + 1] * inv);
+          *reinterpret_cast<uint2*>(dst + 8 * i + 4 * tq) = wv;
         }
       }
       if (lse && tq == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (mx[h] + __log2f(sum[h])) * 0.6931471805599453f;
@@ -355,10 +359,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
       for (int i = 0; i < C::kNT; ++i) {
         if constexpr (!E4M3) {
           *reinterpret_cast<float2*>(dst + 8 * i + 2 * tq) = make_float2(o[i][2 * h] * vdq, o[i][2 * h + 1] * vdq);
-        } else {
-          int mq = i >> 2, ii = i & 3;
-          dst[32 * mq + 8 * tq + ii] = o[i][2 * h] * vdq;
-          dst[32 * mq + 8 * tq + 4 + ii] = o[i][2 * h + 1] * vdq;
+        } else if ((i & 1) == 0) {
+          *reinterpret_cast<float4*>(dst + 8 * i + 4 * tq) =
+              make_float4(o[i][2 * h] * vdq, o[i + 1][2 * h] * vdq, o[i][2 * h + 1] * vdq, o[i + 1][2 * h + 1] * vdq);
         }
       }
       if (tq == 0) *reinterpret_cast<float2*>(part_ml + slot * 2) = make_float2(mx[h], sum[h]);
