@@ -502,12 +502,17 @@ def run_fork(args, world, rank, local):
         step()
     torch.cuda.synchronize(dev)
     barrier(world)
+    clocks = Clocks(local)
+    clocks.start()
+    wall0 = time.time()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
     ms = allmax(world, t0.elapsed_time(t1) / args.steps)
     assert pie.pie_ctx_check(ctx) == 0
     hbm, src = peaks()
@@ -518,6 +523,7 @@ def run_fork(args, world, rank, local):
            "config": {"workload": "fork_spec", "prompt": prompt, "forks": len(segs), "drafts": drafts,
                       "suffix_tokens": w.suffix, "layers": L, "hq": Hq, "hkv": Hkv, "head_dim": D,
                       "l2": "32 layers of K/V (about 0.7 GB per step), larger than L2"},
+           "clocks": clk,
            "rows_per_s": world * rows / (ms * 1e-3),
            "unshared_equivalent_GBps": world * unshared_layer * L / (ms * 1e-3) / 1e9,
            "roofline": {"bound": "hbm", "kernel": "whole fork pass (append, tensor-core shared prefix, decode suffixes, merge)",
@@ -599,8 +605,15 @@ def run_mixed(args, w, world, rank, local):
         assert pie.pie_ctx_check(ctx) == 0
         return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
 
+    clocks = Clocks(local)
+    clocks.start()
+    wall0 = time.time()
     t_chunks = timed(chunk_segs, make(chunk_segs), args.steps)
     t_mixed = timed(main_segs, make(main_segs), args.steps)
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
+    # K/V bytes one attend reads (each key once per working set)
+    chunk_kv = sum(c0 + s[1] for s, c0 in zip(chunk_segs, w.chunk_ctx)) * Hkv * D * esize * 2
     tflops = flops / (t_chunks * 1e-3) / 1e12
     peak, src = tensor_peak()
     res = {"metric": "prefill attend TFLOP/s (causal-exact flops)", "value": tflops, "unit": "TFLOP/s",
@@ -611,7 +624,10 @@ def run_mixed(args, w, world, rank, local):
            "config": {"workload": w.name, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
                       "logit_softcap": args.logit_softcap,
                       "chunks": len(chunk_segs), "chunk_rows": sum(s[1] for s in chunk_segs),
-                      "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1},
+                      "decode_rows": len(w.decode_ctx), "hq": Hq, "hkv": Hkv, "head_dim": D, "layers": 1,
+                      "l2": f"no flush; the chunks read {chunk_kv / 1e6:.0f} MB of K/V per attend and the whole "
+                            f"step {(chunk_kv + dec_keys * Hkv * D * esize * 2) / 1e6:.0f} MB (L2 is 129 MB)"},
+           "clocks": clk,
            "roofline": {"bound": "tensor", "kernel": "prefill_kernel (chunks-only attend)", "achieved": tflops,
                         "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": tflops / peak,
                         "traffic": traffic(f"prefill_kernel {w.name}", ["prefill.cu", "ptx.cuh", "tcgen05.cuh"],
