@@ -25,6 +25,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/pie_attn.h"
 #include "plan.h"
@@ -375,31 +376,60 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
 template <int D>
 __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                              const float* __restrict__ part_acc, const float* __restrict__ part_ml) {
+  // One warp per (merged row, query head).  Lane k holds part k's (m, l)
+  // (32 parts at a time), so the parts' loads are issued together; the
+  // weights reach every lane by shuffle, and each lane accumulates E dims of
+  // the parts' partial outputs with vector loads, four parts in flight.
   int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.n_merge * g.hq) return;
   int i = wid / g.hq, qh = wid % g.hq;
   int row = p.merge_rows[i], np = p.merge_nparts[i], base = p.row_part_base[row];
-  float m = -INFINITY;
-  for (int k = 0; k < np; ++k) m = fmaxf(m, part_ml[(static_cast<int64_t>(base + k) * g.hq + qh) * 2]);
-  float base_m = m == -INFINITY ? 0.f : m;
+  auto ml_at = [&](int k) {
+    return k < np ? *reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(base + k) * g.hq + qh) * 2)
+                  : make_float2(-INFINITY, 0.f);
+  };
+  const float2 ml0 = ml_at(lane);
+  float m = ml0.x;
+  for (int k0 = 32; k0 < np; k0 += 32) m = fmaxf(m, ml_at(k0 + lane).x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float base_m = m == -INFINITY ? 0.f : m;
   constexpr int E = D / 32;
+  using Vec = typename std::conditional<E == 4, float4, float2>::type;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float l = 0.f;
-  for (int k = 0; k < np; ++k) {
-    int64_t slot = static_cast<int64_t>(base + k) * g.hq + qh;
-    float2 ml = *reinterpret_cast<const float2*>(part_ml + slot * 2);
-    float w = ex2(ml.x - base_m);
+  for (int k0 = 0; k0 < np; k0 += 32) {
+    const float2 ml = k0 == 0 ? ml0 : ml_at(k0 + lane);
+    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - base_m);
     l += ml.y * w;
-    const float* a = part_acc + slot * D;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] += a[lane * E + e] * w;
+    const int n = min(32, np - k0);
+    const float* a = part_acc + (static_cast<int64_t>(base + k0) * g.hq + qh) * D + lane * E;
+#pragma unroll 4
+    for (int kk = 0; kk < n; ++kk) {
+      const float wk = __shfl_sync(0xffffffffu, w, kk);
+      const Vec v = *reinterpret_cast<const Vec*>(a + static_cast<int64_t>(kk) * g.hq * D);
+      acc[0] += v.x * wk;
+      acc[1] += v.y * wk;
+      if constexpr (E == 4) {
+        acc[2] += reinterpret_cast<const float4&>(v).z * wk;
+        acc[3] += reinterpret_cast<const float4&>(v).w * wk;
+      }
+    }
   }
-  float inv = l > 0.f ? 1.f / l : 0.f;
-  __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D + lane * E;
+  if constexpr (E == 4) {
+    uint2 wv;
+    wv.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    wv.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = wv;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  }
   if (lse && lane == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (m + __log2f(l)) * 0.6931471805599453f;
 }
 
