@@ -119,6 +119,8 @@ class Clocks:
     def stop(self, t_begin, t_end):
         """Summary of the samples taken between wall-clock t_begin and t_end."""
         if self.proc is None:
+            self.f.close()
+            os.unlink(self.f.name)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.3)
         self.proc.terminate()

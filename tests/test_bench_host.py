@@ -1,0 +1,101 @@
+"""bench.py's host-side helpers on the CPU: the roofline denominators (the
+measured-peaks file or the fallbacks), the DRAM traffic taken from a
+recorded ncu capture (scaled to the launch, and dropped once the kernel's
+sources change), and the summary of the nvidia-smi clock samples taken
+during a timed region."""
+import datetime
+import json
+import os
+import time
+
+import pytest
+
+import bench
+
+
+def _sources(root, files):
+    csrc = root / "paged_kv_attention_working_gb300" / "csrc"
+    csrc.mkdir(parents=True, exist_ok=True)
+    for name, text in files.items():
+        (csrc / name).write_text(text)
+
+
+def test_traffic_is_scaled_to_the_launch_and_dropped_when_sources_change(tmp_path, monkeypatch):
+    _sources(tmp_path, {"k.cu": "kernel v1", "h.cuh": "helpers"})
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"kern w": {"source_sha256": bench.kernel_sources_sha(["k.cu", "h.cuh"]),
+                      "dram_bytes_per_launch": 1000, "algorithmic_per_launch": 500}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.traffic("kern w", ["k.cu", "h.cuh"], 500) == 1000
+    # a capture of a smaller case of the workload, scaled to the full launch
+    assert bench.traffic("kern w", ["k.cu", "h.cuh"], 2000) == 4000
+    assert bench.traffic("another kernel", ["k.cu", "h.cuh"], 500) is None
+    # the hash covers the files in the order given
+    assert bench.traffic("kern w", ["h.cuh", "k.cu"], 500) is None
+    (tmp_path / "paged_kv_attention_working_gb300" / "csrc" / "k.cu").write_text("kernel v2")
+    assert bench.traffic("kern w", ["k.cu", "h.cuh"], 500) is None
+
+
+def test_traffic_without_a_recorded_capture_is_none(tmp_path, monkeypatch):
+    _sources(tmp_path, {"k.cu": "kernel"})
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic("kern w", ["k.cu"], 1) is None
+
+
+@pytest.mark.parametrize("content, hbm, tensor", [
+    (None, (bench.FALLBACK_HBM_GBS, "fallback"), (bench.FALLBACK_BF16_TFLOPS, "fallback")),
+    ({"hbm_gbs": 6698.0, "bf16_tflops": 1929.0, "bf16_tflops_sustained": 1743.5},
+     (6698.0, "measured"), (1929.0, "measured")),
+    ({"hbm_gbs": {"value": 6500}, "bf16_TFLOPs": {"value": 1800.5}}, (6500.0, "measured"), (1800.5, "measured")),
+    ({"hbm_gbs": 0, "bf16_tflops": "n/a"},
+     (bench.FALLBACK_HBM_GBS, "fallback"), (bench.FALLBACK_BF16_TFLOPS, "fallback")),
+    ("{not json", (bench.FALLBACK_HBM_GBS, "fallback"), (bench.FALLBACK_BF16_TFLOPS, "fallback")),
+])
+def test_peaks_are_measured_when_the_file_has_them(tmp_path, monkeypatch, content, hbm, tensor):
+    if content is not None:
+        text = content if isinstance(content, str) else json.dumps(content)
+        (tmp_path / "MEASURED_PEAKS.json").write_text(text)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == hbm
+    assert bench.tensor_peak() == tensor
+
+
+class _StoppedSampler:
+    def terminate(self):
+        pass
+
+    def wait(self):
+        pass
+
+
+def test_clock_summary_keeps_samples_inside_the_timed_region():
+    c = bench.Clocks(0)
+    c.proc = _StoppedSampler()
+    t0 = time.time()
+
+    def row(dt, sm, mx, hw="Not Active", thermal="Not Active", power="Not Active"):
+        ts = datetime.datetime.fromtimestamp(t0 + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {sm}, {mx}, 900.5, 0x0, {hw}, {thermal}, Not Active, {power}\n"
+
+    c.f.write(row(-5.0, 1000, 2070, hw="Active"))     # before the region: ignored
+    c.f.write(row(0.1, 1980, 2070, power="Active"))
+    c.f.write(row(0.3, 2070, 2070))
+    c.f.write(row(0.5, "[N/A]", 2070))                  # unreadable clock: not counted
+    c.f.write(row(0.7, 2070, 2070))
+    c.f.write(row(9.0, 1200, 2070, thermal="Active"))  # after the region: ignored
+    c.f.flush()
+    s = c.stop(t0, t0 + 1.0)
+    assert s["sm_mhz"] == 2070.0
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["samples"] == 4
+    assert not os.path.exists(c.f.name)
+
+
+def test_clock_summary_without_nvidia_smi():
+    c = bench.Clocks(0)
+    c.proc = None
+    s = c.stop(0.0, 1.0)
+    assert s["sm_mhz"] is None and s["reasons"] == ["nvidia-smi unavailable"]
+    assert not os.path.exists(c.f.name)
