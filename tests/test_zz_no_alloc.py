@@ -37,6 +37,9 @@ def _close(got, ref, what):
     ("llama8b_small", dict(name="na8b", seed=21, n_ws=6, ctx_lo=200, ctx_hi=1500, num_layers=2)),
     ("many_rows", dict(name="narows", seed=22, n_ws=48, ctx_lo=1, ctx_hi=700, num_layers=1)),
     ("d64", dict(name="na64", seed=23, n_ws=5, ctx_lo=30, ctx_hi=400, num_layers=1, hq=8, hkv=2, d=64)),
+    # two rows: the entry point splits them into about 60 parts each (empty
+    # ones for the shorter row), which the merge takes 32 at a time
+    ("two_long_rows", dict(name="na2", seed=24, n_ws=2, ctx_lo=2500, ctx_hi=3000, num_layers=1)),
 ])
 def test_noalloc_decode_matches_attend_on_two_calls(name, kw):
     w = wl.decode_batch(**kw)
