@@ -265,6 +265,40 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def decode_attend_bytes(w):
+    """Algorithmic bytes of one decode attend launch (one layer) of a decode
+    workload: K and V of every visible key once per working set (the keys a
+    dedup group shares once per group: w.shared_keys counts the copies
+    beyond the first), Q and O, the LSE and the page ids.  Returns (K/V
+    bytes, whole launch)."""
+    Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+    esize = 2 if w.kv_dtype == 0 else 1
+    n_rows = len(w.ctx)
+    shared = getattr(w, "shared_keys", 0)
+    keys = sum(c + 1 for c in w.ctx) - shared
+    pages = sum(-(-(c + 1) // 16) for c in w.ctx) - shared // 16
+    kv = keys * Hkv * D * esize * 2
+    return kv, kv + 2 * n_rows * Hq * D * 2 + n_rows * Hq * 4 + 4 * pages
+
+
+def prefill_chunk_flops(w, chunk_segs):
+    """Causal-exact flops of the mixed batch's prefill chunks: 4*d per
+    (query head, visible key) pair; a chunk of n rows on c cached tokens has
+    n*c + n(n+1)/2 such pairs per head."""
+    return sum(4 * w.head_dim * w.num_q_heads * (s[1] * c0 + s[1] * (s[1] + 1) // 2)
+               for s, c0 in zip(chunk_segs, w.chunk_ctx))
+
+
+def llama70b_workload(n_ws):
+    """The 70B-shaped FP8 decode batch, n_ws working sets in dedup groups of
+    8 sharing a 2048-token prefix."""
+    from paged_kv_attention_working_gb300 import workloads as wl
+
+    w = wl.llama70b_fp8(n_ws=n_ws, prefix_groups=n_ws // 8)
+    w.shared_keys = (n_ws - n_ws // 8) * 2048   # shared keys beyond their first copy in each group
+    return w
+
+
 # ----------------------------------------------------------------- GPU leg
 def run_gpu(args, w, world, rank, local):
     import torch
@@ -320,13 +354,8 @@ def run_gpu(args, w, world, rank, local):
     lse = torch.empty((L, n_rows, Hq), dtype=torch.float32, device=dev)
     segs = [(hs[n], 1, None) for n in names]
 
-    # algorithmic bytes of one attend launch (one layer): every visible key
-    # once per working set, and pages shared by a dedup group once per group
-    shared = getattr(w, "shared_keys", 0)
-    keys = sum(c + 1 for c in w.ctx) - shared
-    pages = sum(-(-(c + 1) // 16) for c in w.ctx) - shared // 16
-    kv_bytes_layer = keys * Hkv * D * esize * 2
-    attend_bytes = kv_bytes_layer + 2 * n_rows * Hq * D * 2 + n_rows * Hq * 4 + 4 * pages
+    assert n_rows == len(w.ctx)
+    kv_bytes_layer, attend_bytes = decode_attend_bytes(w)
     append_bytes = n_rows * Hkv * D * (2 + esize) * 2
     if args.rope_theta:
         qr = torch.empty_like(q)
@@ -582,10 +611,7 @@ def run_mixed(args, w, world, rank, local):
         return q, kv, out
 
     chunk_segs = [s for s in main_segs if s[0].startswith("c")]
-    flops = 0
-    for s, c0 in zip(chunk_segs, w.chunk_ctx):
-        nn = s[1]
-        flops += 4 * D * Hq * (nn * c0 + nn * (nn + 1) // 2)
+    flops = prefill_chunk_flops(w, chunk_segs)
     dec_keys = sum(c + 1 for c in w.decode_ctx)
 
     # written before every timed attend so that no K/V stays in L2 (129 MB)
@@ -692,10 +718,7 @@ def main():
             print(json.dumps(res), flush=True)
         return
     if args.workload == "llama70b_fp8":
-        n_ws = args.n_ws or 256
-        w = wl.llama70b_fp8(n_ws=n_ws, prefix_groups=n_ws // 8)
-        # keys of the shared dedup prefix beyond their first copy in each group
-        w.shared_keys = (n_ws - n_ws // 8) * 2048
+        w = llama70b_workload(args.n_ws or 256)
     else:
         w = wl.llama8b_decode(num_layers=args.layers)
     if args.impl == "reference":

@@ -99,3 +99,36 @@ def test_clock_summary_without_nvidia_smi():
     s = c.stop(0.0, 1.0)
     assert s["sm_mhz"] is None and s["reasons"] == ["nvidia-smi unavailable"]
     assert not os.path.exists(c.f.name)
+
+
+def test_recorded_captures_match_the_workloads_algorithmic_work():
+    """profiles/traffic.json scales each capture by the algorithmic work of
+    the launch it measured; that work must still be what bench.py computes
+    for the same workload (a change to a workload generator would otherwise
+    scale the recorded traffic wrongly)."""
+    from paged_kv_attention_working_gb300 import workloads as wl
+
+    with open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    w8 = wl.llama8b_decode(num_layers=32)
+    assert bench.decode_attend_bytes(w8)[1] == rec["decode_kernel llama8b_decode"]["algorithmic_per_launch"]
+    # the 70B capture ran 64 of the 256 working sets (8 dedup groups)
+    w70 = bench.llama70b_workload(64)
+    assert bench.decode_attend_bytes(w70)[1] == rec["decode_kernel llama70b_fp8"]["algorithmic_per_launch"]
+    for name in ("mixed_batch", "mixed_batch_e4m3"):
+        w = wl.mixed_batch(name=name, kv_dtype=wl.KV_E4M3 if name.endswith("e4m3") else wl.KV_BF16)
+        main_segs = [op for op in w.ops if op[0] == "pass"][1][1]
+        chunks = [s for s in main_segs if s[0].startswith("c")]
+        assert bench.prefill_chunk_flops(w, chunks) == rec[f"prefill_kernel {name}"]["algorithmic_per_launch"]
+
+
+def test_shared_prefix_bytes_count_each_group_once():
+    """The dedup groups' shared prefix is counted once per group: 56 of the 64
+    working sets reuse their group's 2048-token prefix, so the batch's K/V
+    bytes are those of the unshared batch less 56 prefixes."""
+    from paged_kv_attention_working_gb300 import workloads as wl
+
+    w = bench.llama70b_workload(64)
+    plain = wl.llama70b_fp8(n_ws=64, prefix_groups=8)
+    per_key = w.num_kv_heads * w.head_dim * 1 * 2      # e4m3 K and V
+    assert bench.decode_attend_bytes(plain)[0] - bench.decode_attend_bytes(w)[0] == 56 * 2048 * per_key
