@@ -1,6 +1,6 @@
-"""Benchmark of one batched decode pass over paged KV working sets.
+"""Benchmark of batched passes over paged KV working sets.
 
-Workload (default): Llama-3.1-8B-shaped decode batch -- 64 working sets with
+Headline workload: Llama-3.1-8B-shaped decode batch -- 64 working sets with
 contexts uniform in [512, 8192] (seeded), 32 query / 8 KV heads, head_dim 128,
 bf16 KV in 16-token pages, 32 layers of independent random K/V.  One step is
 one whole pass through the hot path: pie_batch_begin (slot reservation,
@@ -12,6 +12,14 @@ Metric: decode attend KV GB/s = algorithmic K/V bytes the attention reads
 (every valid key once per working set, K and V) / step time; plus query
 rows/s.  Inputs (KV cache, Q/K/V of the step) are resident in HBM; the KV
 read per layer (~1.1 GB) is far larger than L2, so no flush is needed.
+
+The same JSON line carries, under "workloads", the other timed workloads,
+each with its own timing, roofline and clock record: the fork / speculative
+pass (a 4096-token prompt shared by 10 forks), the mixed continuous batch
+(prefill chunks on the tensor cores plus decode rows; bf16 and e4m3 KV) and
+the Llama-3.3-70B-shaped long-context decode with e4m3 KV and dedup groups.
+--workload X runs one of them alone as the headline; --only-headline skips
+the others.
 
 --impl reference times the CPU oracle instead (bounded sample).
 """
@@ -289,6 +297,16 @@ def prefill_chunk_flops(w, chunk_segs):
                for s, c0 in zip(chunk_segs, w.chunk_ctx))
 
 
+def append_roofline(nbytes, avg_ms, peak, peak_src, kernel):
+    """Roofline of one kv_append launch: algorithmic bytes (each new row's K
+    and V read as bf16 and written in the pool's element type; with the
+    rotary embedding also Q read and written and the (cos, sin) pairs) over
+    the event-timed launch."""
+    gbs = nbytes / (avg_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "bytes_per_launch": nbytes, "avg_launch_ms": avg_ms,
+            "achieved": gbs, "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": gbs / peak}
+
+
 def llama70b_workload(n_ws):
     """The 70B-shaped FP8 decode batch, n_ws working sets in dedup groups of
     8 sharing a 2048-token prefix."""
@@ -300,7 +318,7 @@ def llama70b_workload(n_ws):
 
 
 # ----------------------------------------------------------------- GPU leg
-def run_gpu(args, w, world, rank, local):
+def run_gpu(args, w, world, rank, local, e2e=True):
     import torch
 
     from paged_kv_attention_working_gb300 import pie
@@ -372,15 +390,17 @@ def run_gpu(args, w, world, rank, local):
         bb = pie.pie_batch_begin(ctx, segs)
         info.update(pie.pie_batch_plan_info(bb))
         for layer in range(L):
+            if ev is not None:
+                ev[layer][0].record(stream)
             if args.rope_theta:
                 pie.pie_kv_append_rope(ctx, bb, layer, kn[layer], vn[layer], q[layer], qr[layer])
             else:
                 pie.pie_kv_append(ctx, bb, layer, kn[layer], vn[layer])
             if ev is not None:
-                ev[layer][0].record(stream)
+                ev[layer][1].record(stream)
             pie.pie_attend(ctx, bb, layer, qr[layer] if args.rope_theta else q[layer], out[layer], lse[layer])
             if ev is not None:
-                ev[layer][1].record(stream)
+                ev[layer][2].record(stream)
         pie.pie_batch_end(ctx, bb)
         if host is not None:
             oh.copy_(out, non_blocking=True)
@@ -396,7 +416,7 @@ def run_gpu(args, w, world, rank, local):
     time.sleep(0.5)  # let the clock sampler start before the timed region
 
     # ---- device-resident timing
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)] for _ in range(args.steps)]
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.time()
@@ -412,26 +432,32 @@ def run_gpu(args, w, world, rank, local):
     barrier(world)
     ms = t0.elapsed_time(t1) / args.steps
     ms = allmax(world, ms)
-    attend_ms = [e0.elapsed_time(e1) for st in events for e0, e1 in st]
+    attend_ms = [e1.elapsed_time(e2) for st in events for _, e1, e2 in st]
+    append_ms = [e0.elapsed_time(e1) for st in events for e0, e1, _ in st]
     attend_avg = statistics.mean(attend_ms)
+    append_avg = statistics.mean(append_ms)
     assert pie.pie_ctx_check(ctx) == 0
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
-    host = (q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory(),
-            torch.empty(out.shape, dtype=out.dtype).pin_memory())
-    step(host=host)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s in range(args.steps):
+    e2e_res = None
+    if e2e:
+        host = (q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory(),
+                torch.empty(out.shape, dtype=out.dtype).pin_memory())
         step(host=host)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = allmax(world, e0.elapsed_time(e1) / args.steps)
-    h2d = sum(t.numel() * t.element_size() for t in host[:3])
-    d2h = host[3].numel() * host[3].element_size()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            step(host=host)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = allmax(world, e0.elapsed_time(e1) / args.steps)
+        h2d = sum(t.numel() * t.element_size() for t in host[:3])
+        d2h = host[3].numel() * host[3].element_size()
+        e2e_res = {"value": world * kv_bytes_layer * L / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                   "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     hbm_peak, peak_src = peaks()
     kv_step = kv_bytes_layer * L
@@ -455,9 +481,10 @@ def run_gpu(args, w, world, rank, local):
                      "frac": achieved / hbm_peak,
                      "traffic": traffic(f"decode_kernel {w.name}", ["decode.cu", "ptx.cuh"], attend_bytes),
                      "algorithmic_bytes_per_launch": attend_bytes, "avg_launch_ms": attend_avg},
-        "append": {"bytes_per_launch": append_bytes},
-        "e2e": {"value": world * kv_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "append": append_roofline(append_bytes, append_avg, hbm_peak, peak_src,
+                                  "kv_append_rope" if args.rope_theta else
+                                  ("kv_append_bf16" if w.kv_dtype == 0 else "kv_append_e4m3")),
+        "e2e": e2e_res,
         "gpu_launches": args.steps * L * launches_per_layer,
         "clocks": clk,
     }
@@ -520,15 +547,23 @@ def run_fork(args, world, rank, local):
     kv_bytes_layer = (prompt + private) * Hkv * D * 2 * 2
     unshared_layer = (len(segs) * prompt + private) * Hkv * D * 2 * 2
 
-    def step():
+    def step(ev=None):
         bb = pie.pie_batch_begin(ctx, segs)
+        info.update(pie.pie_batch_plan_info(bb))
         for layer in range(L):
+            if ev is not None:
+                ev[layer][0].record(stream)
             pie.pie_kv_append(ctx, bb, layer, kv[layer], kv[layer])
+            if ev is not None:
+                ev[layer][1].record(stream)
             pie.pie_attend(ctx, bb, layer, q[layer], out[layer])
+            if ev is not None:
+                ev[layer][2].record(stream)
         pie.pie_batch_end(ctx, bb)
         for sg in segs:
             pie.pie_ws_rollback(ctx, sg[0], drafts)
 
+    info = {}
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -546,6 +581,15 @@ def run_fork(args, world, rank, local):
     clk = clocks.stop(wall0, wall1)
     ms = allmax(world, t0.elapsed_time(t1) / args.steps)
     assert pie.pie_ctx_check(ctx) == 0
+    # the per-layer split, from separately timed steps (events between the
+    # calls add a little time of their own, so these are not the step time)
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
+              for _ in range(min(args.steps, 10))]
+    for ev in events:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    append_us = 1e3 * statistics.mean(e0.elapsed_time(e1) for st in events for e0, e1, _ in st)
+    attend_us = 1e3 * statistics.mean(e1.elapsed_time(e2) for st in events for _, e1, e2 in st)
     hbm, src = peaks()
     value = world * kv_bytes_layer * L / (ms * 1e-3) / 1e9
     res = {"metric": "fork decode attend KV GB/s (shared prompt read once per pass)", "value": value, "unit": "GB/s",
@@ -557,9 +601,12 @@ def run_fork(args, world, rank, local):
            "clocks": clk,
            "rows_per_s": world * rows / (ms * 1e-3),
            "unshared_equivalent_GBps": world * unshared_layer * L / (ms * 1e-3) / 1e9,
-           "roofline": {"bound": "hbm", "kernel": "whole fork pass (append, tensor-core shared prefix, decode suffixes, merge)",
+           "per_layer_us": {"pass": 1e3 * ms / L, "append": append_us, "attend": attend_us},
+           "plan": info,
+           "roofline": {"bound": "hbm", "kernel": "whole fork pass (append, shared prompt once per pass, "
+                                                  "private suffixes and drafts, merge)",
                         "achieved": value, "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": value / hbm,
-                        "traffic": None}}
+                        "traffic": None, "algorithmic_bytes_per_layer": kv_bytes_layer}}
     pie.pie_ctx_destroy(ctx)
     return res
 
@@ -618,36 +665,44 @@ def run_mixed(args, w, world, rank, local):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def timed(segs, tensors, steps):
+        """Median event-timed attend and append of `steps` passes, L2 flushed
+        before each."""
         q, kv, out = tensors
         evs = []
         for i in range(args.warmup + steps):
             bb = pie.pie_batch_begin(ctx, [(hs[s[0]], s[1], None) for s in segs])
-            pie.pie_kv_append(ctx, bb, 0, kv, kv)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+            e[2].record(stream)
+            pie.pie_kv_append(ctx, bb, 0, kv, kv)
+            e[3].record(stream)
+            flush.zero_()
+            e[0].record(stream)
             pie.pie_attend(ctx, bb, 0, q, out)
-            e1.record(stream)
+            e[1].record(stream)
             pie.pie_batch_end(ctx, bb)
             for s in segs:
                 pie.pie_ws_rollback(ctx, hs[s[0]], s[1])
             if i >= args.warmup:
-                evs.append((e0, e1))
+                evs.append(e)
         torch.cuda.synchronize(dev)
         assert pie.pie_ctx_check(ctx) == 0
-        return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
+        return (statistics.median(e[0].elapsed_time(e[1]) for e in evs),
+                statistics.median(e[2].elapsed_time(e[3]) for e in evs))
 
     clocks = Clocks(local)
     clocks.start()
     wall0 = time.time()
-    t_chunks = timed(chunk_segs, make(chunk_segs), args.steps)
-    t_mixed = timed(main_segs, make(main_segs), args.steps)
+    t_chunks, _ = timed(chunk_segs, make(chunk_segs), args.steps)
+    t_mixed, t_append = timed(main_segs, make(main_segs), args.steps)
     wall1 = time.time()
     clk = clocks.stop(wall0, wall1)
     # K/V bytes one attend reads (each key once per working set)
     chunk_kv = sum(c0 + s[1] for s, c0 in zip(chunk_segs, w.chunk_ctx)) * Hkv * D * esize * 2
     tflops = flops / (t_chunks * 1e-3) / 1e12
     peak, src = tensor_peak()
+    hbm, hsrc = peaks()
+    mixed_rows = sum(s[1] for s in main_segs)
     res = {"metric": "prefill attend TFLOP/s (causal-exact flops)", "value": tflops, "unit": "TFLOP/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_mixed,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -666,11 +721,38 @@ def run_mixed(args, w, world, rank, local):
                         "traffic": traffic(f"prefill_kernel {w.name}", ["prefill.cu", "ptx.cuh", "tcgen05.cuh"],
                                            flops),
                         "flops_per_launch": flops, "avg_launch_ms": t_chunks},
-           "mixed_step": {"attend_ms": t_mixed, "rows": sum(s[1] for s in main_segs),
-                          "rows_per_s": sum(s[1] for s in main_segs) / (t_mixed * 1e-3),
-                          "decode_kv_bytes": dec_keys * Hkv * D * esize * 2}}
+           "mixed_step": {"attend_ms": t_mixed, "rows": mixed_rows,
+                          "rows_per_s": mixed_rows / (t_mixed * 1e-3),
+                          "decode_kv_bytes": dec_keys * Hkv * D * esize * 2},
+           "append": append_roofline(mixed_rows * Hkv * D * (2 + esize) * 2, t_append, hbm, hsrc,
+                                     "kv_append_bf16" if w.kv_dtype == 0 else "kv_append_e4m3")}
     pie.pie_ctx_destroy(ctx)
     return res
+
+
+def slim(res):
+    """A leg's result as a sub-object of the headline line (the keys the
+    headline already states are dropped)."""
+    drop = ("n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data")
+    return {k: v for k, v in res.items() if k not in drop}
+
+
+def other_workloads(args, world, rank, local):
+    """The fork pass, the mixed batch (bf16 and e4m3 KV) and the 70B-shaped
+    FP8 decode, one after the other, each with its own timing and clocks."""
+    import torch
+
+    from paged_kv_attention_working_gb300 import workloads as wl
+
+    out = {}
+    out["fork_spec"] = run_fork(args, world, rank, local)
+    torch.cuda.empty_cache()
+    for name, kv in (("mixed_batch", wl.KV_BF16), ("mixed_batch_e4m3", wl.KV_E4M3)):
+        out[name] = run_mixed(args, wl.mixed_batch(name=name, kv_dtype=kv), world, rank, local)
+        torch.cuda.empty_cache()
+    out["llama70b_fp8"] = run_gpu(args, llama70b_workload(256), world, rank, local, e2e=False)
+    torch.cuda.empty_cache()
+    return {k: slim(v) for k, v in out.items()}
 
 
 def main():
@@ -692,6 +774,8 @@ def main():
                     help="rotary base: K and Q rotated in the append (pie_kv_append_rope); 0 = plain append")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="time the headline workload alone (no fork / mixed / 70B sub-objects)")
     args = ap.parse_args()
     from paged_kv_attention_working_gb300 import workloads as wl
 
@@ -725,6 +809,11 @@ def main():
         run_reference(args, w, world, rank)
         return
     result = run_gpu(args, w, world, rank, local)
+    if args.workload == "llama8b_decode" and not args.only_headline:
+        import torch
+
+        torch.cuda.empty_cache()
+        result["workloads"] = other_workloads(args, world, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
             gbs, rps, desc, cores, _ = OracleSample(w).run(args.ref_seconds)

@@ -15,7 +15,10 @@
  *
  * Conventions
  *  - Every call returns a pie_status: 0 = PIE_OK, negative = error.  A
- *    failed call changes no state; pie_last_error() then describes it.
+ *    failed call changes no host state (working sets, pages, reference
+ *    counts, the open batch); pie_last_error() then describes it.  A CUDA
+ *    failure part-way through enqueuing device work (PIE_ERR_CUDA) may
+ *    leave the work enqueued before it on the stream.
  *  - Handles are opaque.  A context is not thread-safe: one host thread at a
  *    time.
  *  - Device pointers passed in are owned by the caller and only borrowed for
@@ -120,10 +123,22 @@ typedef struct pie_seg {
   const int32_t* token_ids;
 } pie_seg;
 
-/* Context.  Copies the configuration; when k_pool is set, allocates its
- * device buffers (scales, the rotary table when rope_theta > 0, the plan,
- * partial results) with cudaMalloc and creates a second stream and two
- * events of its own. */
+/* Context: the KV space of one model's attention layers and the working
+ * sets over it.  The per-layer, per-KV-head K and V caches follow "Write a
+ * model in Poem", section 4 "State (caches)"; one page id space shared by
+ * all layers follows fold_layers ("Write a model in Poem", section 5
+ * "Forward pass"); grouped-query heads follow "Write a model in Poem",
+ * "Shared building blocks"; the e4m3 cache follows the FP8 deployments of
+ * "Write a model in Poem", section 2 "Deployments".
+ * Copies the configuration; when k_pool is set, allocates its device
+ * buffers (scales, the rotary table when rope_theta > 0, the plan, partial
+ * results) with cudaMalloc and creates a second stream and two events of
+ * its own.  PIE_ERR_INVALID for: a non-positive count, page_size != 16,
+ * Hq not a multiple of Hkv, Hq/Hkv not a power of two <= 64, head_dim not
+ * 64 or 128 (bf16) or 128 (e4m3), only one of k_pool / v_pool, missing or
+ * non-positive e4m3 scales, a free_list that is not a permutation, a
+ * negative or non-finite logit_softcap, or rope_theta in (0, 1].
+ * PIE_ERR_CUDA if a device allocation fails (nothing is kept). */
 pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out);
 /* Synchronises the streams, frees everything the context allocated. */
 pie_status pie_ctx_destroy(pie_ctx* ctx);
@@ -154,15 +169,27 @@ pie_status pie_ws_rollback(pie_ctx* ctx, pie_ws ws, int32_t n);
  * tokens become frozen.  *n_reused = matched tokens (a multiple of 16). */
 pie_status pie_ws_match_prefix(pie_ctx* ctx, pie_ws ws, const int32_t* token_ids,
                                int32_t n, int32_t* n_reused);
+/* Introspection of the working-set state of "How Pie thinks", section 4
+ * (tokens, the frozen prefix, and the pages holding them; fork and dedup
+ * share pages, so a page's reference count is the number of working sets
+ * whose table holds it).  Host only; any output pointer may be NULL.
+ * Unknown handle: PIE_ERR_BAD_HANDLE. */
 pie_status pie_ws_info(const pie_ctx* ctx, pie_ws ws, int32_t* n_tokens,
                        int32_t* n_frozen, int32_t* n_pages);
 /* Copies up to cap physical page ids (logical order) into out; *n = count. */
 pie_status pie_ws_page_table(const pie_ctx* ctx, pie_ws ws, int32_t* out,
                              int32_t cap, int32_t* n);
+/* Reference count of a page (0 = free); page out of range: PIE_ERR_INVALID. */
 pie_status pie_page_refcount(const pie_ctx* ctx, int32_t page, int32_t* rc);
 pie_status pie_free_pages(const pie_ctx* ctx, int32_t* n_free);
 
 /* ---- one batched pass ----
+ * The runtime packs the passes of many working sets into shared kernel
+ * launches ("How Pie thinks", "Batching is still the engine's job"), and
+ * the plan of a pass is built once for all layers (ops.attn.plan_prefill in
+ * "Poem ops", Operations table; fold_layers in "Write a model in Poem",
+ * section 5).  New tokens enter a working set's writable buffer ("How Pie
+ * thinks", section 4).
  * Rows are the new tokens of all segments, in segment order, then token
  * order.  Each working set may appear once.  Reserves a slot for every row
  * (allocating pages segment by segment, token by token; a write into a
@@ -171,7 +198,10 @@ pie_status pie_free_pages(const pie_ctx* ctx, int32_t* n_free);
  * host-to-device copy and enqueues the copy-on-write page copies on the
  * stream.  The new tokens become writable tokens of their working sets.
  * Fails with PIE_ERR_NO_PAGES, changing nothing, if the pool cannot cover
- * the whole pass.  One batch may be open per context. */
+ * the whole pass.  Fails with PIE_ERR_CUDA if a device buffer cannot grow
+ * or the upload or the page-copy launch cannot be enqueued; the slots it
+ * had reserved are released again and the host state is as before the
+ * call.  One batch may be open per context. */
 pie_status pie_batch_begin(pie_ctx* ctx, const pie_seg* segs, int32_t n_segs,
                            pie_batch** out);
 /* Number of rows of the batch. */
@@ -235,13 +265,18 @@ pie_status pie_batch_end(pie_ctx* ctx, pie_batch* b);
  * pie_attend.  KV splits and their partial results live in one file-scope
  * device array of PIE_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
  * library holds until the process exits.
- *  - Scratch needed, with S = the KV splits the call picks (S >= 1):
- *      R*32 + 5*R*4 + (S > 1 ? R*S*(32 + Hq*(head_dim+2)*4) : 0) bytes plus
- *    alignment; the call lowers S to fit and returns PIE_ERR_RANGE, with
- *    nothing launched, when even S = 1 does not fit.
+ *  - Scratch needed, with R = num_rows and S = the KV splits the call picks
+ *    (S >= 1): R*S*32 + 5*R*4 + (S > 1 ? R*S*Hq*(head_dim+2)*4 : 0) bytes
+ *    plus alignment; the call lowers S to fit and returns PIE_ERR_RANGE,
+ *    with nothing launched, when even S = 1 does not fit.
+ *  - The splits are sized from max_pages_per_row, so keep it tight (the
+ *    longest row's page count): a wider row stride gives every row more
+ *    empty splits, which cost launch slots and merge reads but not accuracy.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the process, so
+ *    calls after a cudaDeviceReset (or any teardown of the device's primary
+ *    context) are not supported.
  *  - Every call on a device shares the array and leaves its contents behind;
  *    nothing in it needs to start at zero, because each call writes every
  *    word it reads before reading it.  Calls that overlap on the GPU (other
@@ -290,6 +325,12 @@ pie_status pie_ctx_check(pie_ctx* ctx, int32_t* flags);
  * complete, bounded at `polls` polls; it records bit 0 in the error word
  * (read it with pie_ctx_check) and ends.  The context stays usable. */
 pie_status pie_selftest_wait_timeout(pie_ctx* ctx, int32_t polls);
+/* Error-path self-test on the host: the next pie_batch_begin that passes
+ * its argument and page-count checks fails with PIE_ERR_CUDA where it would
+ * upload its plan -- after reserving its slots, as a real CUDA failure
+ * there would -- so that tests can check that the reservation is undone.
+ * Also works on plan-only contexts. */
+pie_status pie_selftest_fail_next_begin(pie_ctx* ctx);
 
 #ifdef __cplusplus
 }

@@ -28,6 +28,7 @@
 #include <type_traits>
 
 #include "../../include/pie_attn.h"
+#include "func_attr.h"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -86,18 +87,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      bool ok = true;
+      int issued = 0;
       for (int j = 0; j < it.n_pages; ++j) {
         int s = j % C::kStages;
-        if (j >= C::kStages && ok) ok = mbar_wait(&empty[s], ((j / C::kStages) - 1) & 1, err);
-        if (!ok) break;
+        if (j >= C::kStages && !mbar_wait(&empty[s], ((j / C::kStages) - 1) & 1, err)) break;
         int page = p.page_ids[it.pages_off + j];
         int64_t boff = (layer_blk + static_cast<int64_t>(page) * g.hkv + head) * C::kBlock;
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], 2 * C::kBlock);
         bulk_g2s(st, kpool + boff, C::kBlock, &full[s]);
         bulk_g2s(st + C::kBlock, vpool + boff, C::kBlock, &full[s]);
+        issued = j + 1;
       }
+      // Before this thread leaves, the copies it issued into the last stages
+      // have landed (bounded): the consumers already waited for them unless
+      // a wait of theirs ran out, and then no copy may outlive the CTA.
+      for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
+        if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, err)) break;
     }
     return;
   }
@@ -158,12 +164,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
 #pragma unroll
   for (int i = 0; i < C::kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float mx[2] = {-INFINITY, -INFINITY}, sum[2] = {0.f, 0.f};
-  bool ok = true;
 
   for (int j = grp; j < it.n_pages; j += n_grp) {
     const int s = j % C::kStages;
-    if (ok) ok = mbar_wait(&full[s], (j / C::kStages) & 1, err);
-    if (!ok) break;
+    // warp-uniform: the shuffles and MMAs below need every lane
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / C::kStages) & 1, err))) break;
     const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
     const uint32_t vb = kb + C::kBlock;
 
@@ -438,13 +443,8 @@ cudaError_t launch_decode_t(const Geometry& g, const PlanView& p, int layer, con
                             const void* vpool, const float* ks, const float* vs, void* out, float* lse,
                             float* acc, float* ml, int* err, cudaStream_t st) {
   using C = DecodeCfg<E4M3, D>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<E4M3, D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = ensure_smem_attr<decode_kernel<E4M3, D, CAP>>(C::kSmem);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.n_dec, g.hkv);
   decode_kernel<E4M3, D, CAP><<<grid, kThreads, C::kSmem, st>>>(
       g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),

@@ -105,6 +105,7 @@ struct pie_ctx {
   float* d_part = nullptr;  // partial (acc | m,l) results
   size_t part_cap = 0;      // floats
   pie_batch* open = nullptr;
+  bool fail_next_begin = false;  // self-test: fake a CUDA failure at the plan upload
 };
 
 namespace {
@@ -366,6 +367,37 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
     return a.n_pages > b.n_pages;
   });
   std::stable_sort(pb.pre.begin(), pb.pre.end(), longer);
+}
+
+// What pie_batch_begin changed in the host state, in order: per segment the
+// working set's length and page count before the pass (and the shared tail
+// page a copy-on-write replaced), and every page taken from the free stack.
+struct Undo {
+  struct Seg {
+    pie_ws ws;
+    int32_t n_tokens, n_pages, cow_tail;
+  };
+  std::vector<Seg> segs;
+  std::vector<int32_t> allocated;
+};
+
+// Puts the host state back as it was before the reservation: tokens and
+// pages dropped, shared tails restored, and the pages returned to the free
+// stack in reverse order of allocation, so the stack's order is unchanged.
+void undo_reservation(pie_ctx* c, const Undo& u) {
+  for (auto it = u.segs.rbegin(); it != u.segs.rend(); ++it) {
+    WorkingSet& w = c->ws[it->ws];
+    w.tokens.resize(it->n_tokens);
+    w.pages.resize(it->n_pages);
+    if (it->cow_tail >= 0) {
+      w.pages[it->n_tokens / kPageSize] = it->cow_tail;
+      c->refcount[it->cow_tail] += 1;
+    }
+  }
+  for (auto it = u.allocated.rbegin(); it != u.allocated.rend(); ++it) {
+    c->refcount[*it] = 0;
+    c->free_stack.push_back(*it);
+  }
 }
 
 template <class T>
@@ -651,12 +683,14 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
                 c->free_stack.size());
   if (n_rows > INT32_MAX / 2) return fail(c, PIE_ERR_INVALID, "too many rows");
 
-  // reserve slots
+  // reserve slots; `undo` records what changes, so that a failure further
+  // down (a CUDA call) can put the host state back as it was
   auto* b = new pie_batch();
   b->ctx = c;
   b->n_rows = static_cast<int32_t>(n_rows);
   PlanBuilder pb;
   std::vector<SegInfo> infos;
+  Undo undo;
   b->row_pos.reserve(n_rows);
   b->row_slot.reserve(n_rows);
   for (int32_t i = 0; i < n_segs; ++i) {
@@ -664,13 +698,16 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     if (s.n_new == 0) continue;
     WorkingSet& w = c->ws[s.ws];
     int32_t n0 = w.n_tokens();
+    undo.segs.push_back({s.ws, n0, static_cast<int32_t>(w.pages.size()), -1});
     if (n0 % kPageSize) {
       int32_t tail = w.pages[n0 / kPageSize];
       if (c->refcount[tail] > 1) {
         int32_t fresh = alloc_page(c);
+        undo.allocated.push_back(fresh);
         c->refcount[tail] -= 1;
         w.pages[n0 / kPageSize] = fresh;
         pb.copies.push_back({tail, fresh});
+        undo.segs.back().cow_tail = tail;
       }
     }
     SegInfo si{};
@@ -681,7 +718,10 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     si.group = -1;
     for (int32_t t = 0; t < s.n_new; ++t) {
       int32_t pos = n0 + t;
-      if (pos % kPageSize == 0) w.pages.push_back(alloc_page(c));
+      if (pos % kPageSize == 0) {
+        w.pages.push_back(alloc_page(c));
+        undo.allocated.push_back(w.pages.back());
+      }
       b->row_pos.push_back(pos);
       b->row_slot.push_back(w.pages[pos / kPageSize] * kPageSize + pos % kPageSize);
     }
@@ -714,6 +754,12 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
   v.n_pre = static_cast<int32_t>(pb.pre.size());
   v.n_merge = static_cast<int32_t>(pb.merge_rows.size());
   v.n_copies = static_cast<int32_t>(pb.copies.size());
+  if (c->fail_next_begin) {
+    c->fail_next_begin = false;
+    undo_reservation(c, undo);
+    delete b;
+    return fail(c, PIE_ERR_CUDA, "plan upload: failure injected by pie_selftest_fail_next_begin");
+  }
   if (!c->plan_only && !blob.empty()) {
     pie_status st = ensure_device(c, &c->d_plan, &c->plan_cap, blob.size());
     size_t part_need = static_cast<size_t>(total_parts) * c->geo.hq * (c->geo.d + 2);
@@ -740,9 +786,8 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
       c->upload_pending = e == cudaSuccess;
     }
     if (st != PIE_OK) {
-      // The host state already moved; a CUDA failure here leaves the
-      // context unusable for device work, which the error reports.
-      c->open = b;
+      undo_reservation(c, undo);
+      delete b;
       return st;
     }
     uint8_t* d = c->d_plan;
@@ -759,7 +804,10 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     if (v.n_copies) {
       cudaError_t e = pie::launch_page_copy(c->geo, v, c->cfg.k_pool, c->cfg.v_pool, c->stream);
       if (e != cudaSuccess) {
-        c->open = b;
+        // The plan upload is enqueued, but nothing reads it before the next
+        // pie_batch_begin, which waits for it (upload_pending).
+        undo_reservation(c, undo);
+        delete b;
         return cuda_fail(c, e, "page copy launch");
       }
     }
@@ -881,6 +929,12 @@ pie_status pie_selftest_wait_timeout(pie_ctx* c, int32_t polls) {
   if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
   cudaError_t e = pie::launch_wait_selftest(c->d_err, static_cast<uint32_t>(polls), c->stream);
   if (e != cudaSuccess) return cuda_fail(c, e, "self-test launch");
+  return PIE_OK;
+}
+
+pie_status pie_selftest_fail_next_begin(pie_ctx* c) {
+  if (!c) return PIE_ERR_INVALID;
+  c->fail_next_begin = true;
   return PIE_OK;
 }
 

@@ -48,6 +48,7 @@
 
 #include <cmath>
 
+#include "func_attr.h"
 #include "plan.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -76,7 +77,7 @@ struct PreCfg {
   static constexpr int kOffV = kOffK + kKStages * kKVTile;
   static constexpr int kOffRaw = kOffV + kVStages * kKVTile;
   static constexpr int kOffBar = kOffRaw + kRawStages * kRawTile;
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 * kRawStages;
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 * kRawStages + 1;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
   uint64_t* o_done = p_full + 2;                  // [tile]: PV_t(j) complete
   uint64_t* raw_full = o_done + 2;                // [raw stage] (e4m3 only)
   uint64_t* raw_empty = raw_full + C::kRawStages;
+  uint64_t* mma_drain = raw_empty + C::kRawStages;  // every issued MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const WorkItem it = p.pre_items[blockIdx.x];
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
       mbar_init(&p_full[t], 4);
       mbar_init(&o_done[t], 1);
     }
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
   // Q tiles -> shared memory, 128-byte swizzled K-major; rows past M are zero
@@ -238,11 +241,10 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     // Raw tiles in order K(0), V(0), K(1), V(1), ...: one 2-KB page block
     // per lane 0..7 into the staging ring.
     const int64_t layer_blk = static_cast<int64_t>(layer) * g.num_pages * g.hkv;
-    bool ok = true;
-    for (int i = 0; i < 2 * nkv && ok; ++i) {
+    int issued = 0;
+    for (int i = 0; i < 2 * nkv; ++i) {
       const int r = i % C::kRawRing, j = i >> 1;
-      if (i >= C::kRawRing) ok = warp_wait(&raw_empty[r], ((i / C::kRawRing) - 1) & 1, err);
-      if (!ok) break;
+      if (i >= C::kRawRing && !warp_wait(&raw_empty[r], ((i / C::kRawRing) - 1) & 1, err)) break;
       if (lane == 0) mbar_arrive_expect_tx(&raw_full[r], C::kRawTile);
       __syncwarp();
       if (lane < C::kPagesPerTile) {
@@ -254,7 +256,11 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
                  &raw_full[r]);
       }
       __syncwarp();
+      issued = i + 1;
     }
+    // no copy outlives the CTA, even when a consumer's wait ran out
+    for (int i = issued > C::kRawRing ? issued - C::kRawRing : 0; i < issued; ++i)
+      if (!warp_wait(&raw_full[i % C::kRawRing], (i / C::kRawRing) & 1, err)) break;
   } else if (E4M3 && warp >= 10) {
     // ------------------------------------------------ converters (e4m3)
     // Raw page block pg holds key s's 16-byte chunk c (dims 16c..16c+15) at
@@ -326,11 +332,10 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
       return lane < ncopy ? p.page_ids[it.pages_off + pj] : 0;
     };
     int page = nkv > 0 ? page_of(0) : 0;
-    bool ok = true;
-    for (int j = 0; j < nkv && ok; ++j) {
+    int issued = 0;
+    for (int j = 0; j < nkv; ++j) {
       const int st = j % nst;
-      if (j >= nst) ok = warp_wait(&empty[st], ((j / nst) - 1) & 1, err);
-      if (!ok) break;
+      if (j >= nst && !warp_wait(&empty[st], ((j / nst) - 1) & 1, err)) break;
       if (lane == 0) mbar_arrive_expect_tx(&full[st], C::kKVTile);
       __syncwarp();
       if (lane < ncopy) {
@@ -346,7 +351,11 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
       }
       if (j + 1 < nkv) page = page_of(j + 1);
       __syncwarp();
+      issued = j + 1;
     }
+    // no copy outlives the CTA, even when a consumer's wait ran out
+    for (int j = issued > nst ? issued - nst : 0; j < issued; ++j)
+      if (!warp_wait(&full[j % nst], (j / nst) & 1, err)) break;
   } else if (warp == 8) {
     // ----------------------------------------------------------------- MMA
     // One thread issues everything, event-driven, PVs first (they gate the
@@ -406,6 +415,10 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
         idle = progressed ? 0 : idle + 1;
       }
       if (idle >= kWaitLimit && err) atomicOr(err, kErrWaitTimeout);
+      // Tensor memory is freed only after every MMA issued here has
+      // completed (normally they have: the softmax warps waited for them).
+      tc::commit(mma_drain);
+      mbar_wait(mma_drain, 0, err);
     }
     __syncwarp();
   } else if (warp / 4 < n_qt) {
@@ -555,13 +568,8 @@ cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void
                      float* ml, int* err, cudaStream_t st) {
   using C = PreCfg<D, E4M3>;
   static_assert(C::kSmem <= 227 * 1024, "shared memory budget");
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<D, E4M3, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = ensure_smem_attr<prefill_kernel<D, E4M3, CAP>>(C::kSmem);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.n_pre, g.hkv);
   prefill_kernel<D, E4M3, CAP><<<grid, C::kThreads, C::kSmem, st>>>(
       g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),

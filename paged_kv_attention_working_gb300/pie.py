@@ -30,7 +30,7 @@ EXPORTS = [
     "pie_ws_page_table", "pie_page_refcount", "pie_free_pages", "pie_batch_begin", "pie_batch_rows",
     "pie_batch_slots", "pie_kv_append", "pie_attend", "pie_batch_end", "pie_batch_plan_info",
     "pie_batch_items", "pie_ctx_check", "pie_attend_decode_noalloc", "pie_selftest_wait_timeout",
-    "pie_kv_append_rope", "pie_rope_table",
+    "pie_kv_append_rope", "pie_rope_table", "pie_selftest_fail_next_begin",
 ]
 PIE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -100,6 +100,7 @@ def _load():
         "pie_ctx_check": [V, P(I)],
         "pie_attend_decode_noalloc": [P(pie_decode_args)],
         "pie_selftest_wait_timeout": [V, I],
+        "pie_selftest_fail_next_begin": [V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -181,6 +182,10 @@ def pie_ctx_check(ctx) -> int:
 
 def pie_selftest_wait_timeout(ctx, polls) -> None:
     _check(ctx, lib.pie_selftest_wait_timeout(ctx, polls), "pie_selftest_wait_timeout")
+
+
+def pie_selftest_fail_next_begin(ctx) -> None:
+    _check(ctx, lib.pie_selftest_fail_next_begin(ctx), "pie_selftest_fail_next_begin")
 
 
 # ------------------------------------------------------------- working sets

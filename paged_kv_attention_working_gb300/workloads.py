@@ -370,7 +370,10 @@ EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_bat
          "llama70b_fp8_softcap", "tiny_decode_softcap", "fork_spec_softcap",
          "mixed_batch_rope", "llama70b_fp8_rope", "fork_spec_rope", "tiny_decode_rope",
          "mixed_batch_d64", "mixed_batch_d64_softcap", "mixed_batch_g8", "mixed_batch_e4m3_g8", "mixed_batch_mha",
-         "edge_batch", "edge_batch_e4m3")
+         "edge_batch", "edge_batch_e4m3",
+         "mixed_batch_g16", "mixed_batch_e4m3_g16", "mixed_batch_mqa_g32", "mixed_batch_mqa_g64",
+         "mixed_batch_e4m3_mqa_g64", "mixed_batch_d64_mqa_g16", "fork_spec_g16", "fork_spec_mqa_g32",
+         "llama70b_fp8_g16", "llama70b_fp8_mqa_g32")
 SOFTCAP_TEST = 3.0
 ROPE_THETA = 500000.0
 
@@ -419,6 +422,40 @@ def reduced(name: str) -> Workload:
     if name == "mixed_batch_mha":
         return mixed_batch(name="mixed_batch_mha_small", seed=22, n_chunks=3, chunk_lo=100, chunk_hi=300,
                            ctx_lo=0, ctx_hi=400, n_decode=5, dec_lo=1, dec_hi=400, hq=8, hkv=8, d=128)
+    # larger head groups: G = 16, 32, 64 query heads per KV head, with one KV
+    # head (multi-query attention) for G = 32 and 64.  Decode rows then fill
+    # 1, 2 or 4 MMA row tiles of the decode kernel, and a tensor-core row
+    # tile holds 16, 8 or 4 rows.
+    if name in ("mixed_batch_g16", "mixed_batch_e4m3_g16", "mixed_batch_mqa_g32", "mixed_batch_mqa_g64",
+                "mixed_batch_e4m3_mqa_g64", "mixed_batch_d64_mqa_g16"):
+        hq, hkv, d = {"mixed_batch_g16": (32, 2, 128), "mixed_batch_e4m3_g16": (32, 2, 128),
+                      "mixed_batch_mqa_g32": (32, 1, 128), "mixed_batch_mqa_g64": (64, 1, 128),
+                      "mixed_batch_e4m3_mqa_g64": (64, 1, 128), "mixed_batch_d64_mqa_g16": (16, 1, 64)}[name]
+        e4 = "e4m3" in name
+        seed = 40 + sorted(EXTRA).index(name)
+        return mixed_batch(name=name + "_small", seed=seed, n_chunks=3, chunk_lo=30, chunk_hi=90,
+                           ctx_lo=0, ctx_hi=300, n_decode=5, dec_lo=1, dec_hi=400, hq=hq, hkv=hkv, d=d,
+                           kv_dtype=KV_E4M3 if e4 else KV_BF16)
+    if name == "fork_spec_g16":
+        # shared prompt: 40 rows x 16 heads on the tensor-core kernel (three
+        # row tiles); each fork's drafts: 4 x 16 = 64, the decode kernel's
+        # largest item
+        return fork_spec(name="fork_spec_g16_small", seed=50, prompt=400, n_forks=10, suffix_hi=40,
+                         hq=32, hkv=2)
+    if name == "fork_spec_mqa_g32":
+        # 4 drafts x 32 heads = 128: the forks' private pages also go to the
+        # tensor-core kernel
+        return fork_spec(name="fork_spec_mqa_g32_small", seed=51, prompt=400, n_forks=10, suffix_hi=40,
+                         hq=32, hkv=1)
+    if name == "llama70b_fp8_g16":
+        # dedup groups of 4 rows x 16 heads = 64 on the decode kernel's shared items
+        return decode_batch(name="llama70b_fp8_g16_small", seed=52, n_ws=8, ctx_lo=300, ctx_hi=1200,
+                            num_layers=1, hq=32, hkv=2, d=128, kv_dtype=KV_E4M3, prefix_groups=2, prefix_len=160)
+    if name == "llama70b_fp8_mqa_g32":
+        # dedup groups of 2 rows x 32 heads = 64, one KV head
+        return decode_batch(name="llama70b_fp8_mqa_g32_small", seed=53, n_ws=8, ctx_lo=300, ctx_hi=1200,
+                            num_layers=1, hq=32, hkv=1, d=128, kv_dtype=KV_E4M3, prefix_groups=4,
+                            prefix_len=160)
     if name == "edge_batch":
         return edge_batch()
     if name == "edge_batch_e4m3":

@@ -106,6 +106,74 @@ def test_random_operation_sequences_bit_exact():
         t.close()
 
 
+def test_failed_begin_leaves_host_state_unchanged():
+    """A pass whose device half fails (a CUDA failure faked on the host at
+    the plan upload, after the slots were reserved) gives PIE_ERR_CUDA and
+    undoes its reservation: page tables, reference counts, the free stack's
+    order (the next allocations match the oracle's) and the lengths are as
+    before, and no batch stays open."""
+    rng = np.random.default_rng(77)
+    for trial in range(12):
+        P = int(rng.integers(8, 48))
+        t = Twin(P, rng.permutation(P).tolist())
+        live = [t.call("ws_create") for _ in range(3)]
+        for step in range(60):
+            op = int(rng.integers(0, 5))
+            segs = []
+            for h in rng.permutation(live)[: rng.integers(1, len(live) + 1)]:
+                n = int(rng.integers(0, 24))
+                segs.append((int(h), n, rng.integers(0, 2, n).tolist() if rng.random() < 0.5 else None))
+            if op == 0:
+                pie.pie_selftest_fail_next_begin(t.c)
+                with pytest.raises(pie.PieError) as e:
+                    pie.pie_batch_begin(t.c, segs)
+                # a pass the pool cannot cover fails before it reserves anything
+                assert e.value.status in (pie.PIE_ERR_CUDA, pie.PIE_ERR_NO_PAGES)
+                if e.value.status == pie.PIE_ERR_NO_PAGES:
+                    # the injected failure is still pending: an empty pass takes it
+                    with pytest.raises(pie.PieError) as e:
+                        pie.pie_batch_begin(t.c, [])
+                    assert e.value.status == pie.PIE_ERR_CUDA
+            elif op == 1:
+                t.call("begin", segs)
+            elif op == 2:
+                h = t.call("ws_fork", live[rng.integers(len(live))])
+                if h is not None:
+                    live.append(h)
+            elif op == 3:
+                t.call("ws_freeze", live[rng.integers(len(live))], int(rng.integers(-1, 30)))
+            else:
+                t.call("ws_rollback", live[rng.integers(len(live))], int(rng.integers(0, 20)))
+            t.compare()
+        t.close()
+
+
+def test_block_offsets_match_hand_worked_header_examples():
+    """The oracle's byte placement inside a page block against offsets worked
+    by hand from the layout the header states (panels of 128 bytes per key,
+    2048 bytes per panel, 16-byte chunk c of slot s at s*128 + 16*(c ^ s%8))."""
+    bf16 = kvstore.block_offsets(16, 128, 2)        # 256 bytes per key: two panels
+    # slot 3, dim 70 -> bytes 140, 141: panel 1, chunk 0 (stored at chunk 3), byte 12
+    assert bf16[3, 140] == 2048 + 3 * 128 + 16 * 3 + 12 == 2492
+    assert bf16[3, 141] == 2493
+    # slot 0 is stored unswizzled: byte b of panel 0 at b
+    assert list(bf16[0, :128]) == list(range(128))
+    # slot 9, byte 17 (dim 8): panel 0, chunk 1 -> chunk 1 ^ 1 = 0, byte 1
+    assert bf16[9, 17] == 9 * 128 + 0 + 1 == 1153
+    # slot 15, last byte (dim 127, high byte): panel 1, chunk 7 -> 7 ^ 7 = 0, byte 15
+    assert bf16[15, 255] == 2048 + 15 * 128 + 15 == 3983
+    e4 = kvstore.block_offsets(16, 128, 1)           # 128 bytes per key: one panel
+    # slot 6, dim 100: chunk 6 -> 6 ^ 6 = 0, byte 4
+    assert e4[6, 100] == 6 * 128 + 4 == 772
+    # slot 13, dim 33: chunk 2 -> 2 ^ 5 = 7, byte 1
+    assert e4[13, 33] == 13 * 128 + 112 + 1 == 1777
+    d64 = kvstore.block_offsets(16, 64, 2)           # 128 bytes per key
+    assert d64[2, 127] == 2 * 128 + 16 * (7 ^ 2) + 15 == 351
+    # every block byte is used exactly once
+    for offs in (bf16, e4, d64):
+        assert sorted(offs.reshape(-1).tolist()) == list(range(offs.size))
+
+
 @pytest.mark.parametrize("name", list(wl.FULL) + list(wl.EXTRA))
 def test_workload_scripts_bit_exact(name):
     w = wl.reduced(name)
