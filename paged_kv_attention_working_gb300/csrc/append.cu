@@ -10,7 +10,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "launch.h"
 #include "plan.h"
+#include "ptx.cuh"
 
 namespace pie {
 namespace {
@@ -28,6 +30,8 @@ __device__ __forceinline__ int64_t slot_chunk_offset(const Geometry& g, int laye
 __global__ void kv_append_bf16(Geometry g, PlanView p, int layer, const uint4* __restrict__ k,
                                const uint4* __restrict__ v, uint8_t* __restrict__ kpool,
                                uint8_t* __restrict__ vpool) {
+  pdl_wait();
+  pdl_trigger();
   const int chunks = g.d * 2 / 16;
   int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   int64_t total = static_cast<int64_t>(p.n_rows) * g.hkv * chunks;
@@ -57,6 +61,8 @@ __global__ void kv_append_e4m3(Geometry g, PlanView p, int layer, const uint4* _
                                const uint4* __restrict__ v, uint8_t* __restrict__ kpool,
                                uint8_t* __restrict__ vpool, const float* __restrict__ inv_k,
                                const float* __restrict__ inv_v) {
+  pdl_wait();
+  pdl_trigger();
   const int chunks = g.d / 16;
   int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   int64_t total = static_cast<int64_t>(p.n_rows) * g.hkv * chunks;
@@ -125,6 +131,8 @@ __global__ void kv_append_rope(Geometry g, PlanView p, int layer, const uint4* _
                                const float* __restrict__ rope, uint8_t* __restrict__ kpool,
                                uint8_t* __restrict__ vpool, const float* __restrict__ inv_k,
                                const float* __restrict__ inv_v) {
+  pdl_wait();
+  pdl_trigger();
   const int nc = g.d / 32;        // 16-dimension groups per half
   const int hd = g.d / 8;         // 16-byte chunks per head row
   const int heads = g.hkv + (q ? g.hq : 0);
@@ -192,6 +200,8 @@ __global__ void kv_append_rope(Geometry g, PlanView p, int layer, const uint4* _
 // A page's blocks for all heads are contiguous, so one page of one layer is
 // hkv * block_bytes consecutive bytes.
 __global__ void page_copy(Geometry g, PlanView p, uint8_t* __restrict__ kpool, uint8_t* __restrict__ vpool) {
+  pdl_wait();
+  pdl_trigger();
   int ci = blockIdx.x / g.num_layers, layer = blockIdx.x % g.num_layers;
   uint8_t* pool = blockIdx.y ? vpool : kpool;
   CopyItem cp = p.copies[ci];
@@ -211,15 +221,15 @@ cudaError_t launch_kv_append(const Geometry& g, const PlanView& p, int layer, co
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
+  cudaError_t e;
   if (g.kv_dtype == 0)
-    kv_append_bf16<<<blocks, threads, 0, st>>>(g, p, layer, static_cast<const uint4*>(k),
-                                                static_cast<const uint4*>(v), static_cast<uint8_t*>(kpool),
-                                                static_cast<uint8_t*>(vpool));
+    e = launch_pdl(kv_append_bf16, blocks, threads, 0, st, g, p, layer, static_cast<const uint4*>(k),
+                   static_cast<const uint4*>(v), static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool));
   else
-    kv_append_e4m3<<<blocks, threads, 0, st>>>(g, p, layer, static_cast<const uint4*>(k),
-                                                static_cast<const uint4*>(v), static_cast<uint8_t*>(kpool),
-                                                static_cast<uint8_t*>(vpool), inv_scale_k, inv_scale_v);
-  return cudaGetLastError();
+    e = launch_pdl(kv_append_e4m3, blocks, threads, 0, st, g, p, layer, static_cast<const uint4*>(k),
+                   static_cast<const uint4*>(v), static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool),
+                   inv_scale_k, inv_scale_v);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_kv_append_rope(const Geometry& g, const PlanView& p, int layer, const void* k, const void* v,
@@ -231,23 +241,20 @@ cudaError_t launch_kv_append_rope(const Geometry& g, const PlanView& p, int laye
   const int threads = 256;
   unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
   auto args = [&](auto kern) {
-    kern<<<blocks, threads, 0, st>>>(g, p, layer, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
-                                     static_cast<const uint4*>(q), static_cast<uint4*>(q_out), rope,
-                                     static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool), inv_scale_k,
-                                     inv_scale_v);
+    return launch_pdl(kern, blocks, threads, 0, st, g, p, layer, static_cast<const uint4*>(k),
+                      static_cast<const uint4*>(v), static_cast<const uint4*>(q), static_cast<uint4*>(q_out), rope,
+                      static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool), inv_scale_k, inv_scale_v);
   };
-  if (g.kv_dtype == 0)
-    args(kv_append_rope<false>);
-  else
-    args(kv_append_rope<true>);
-  return cudaGetLastError();
+  const cudaError_t e = g.kv_dtype == 0 ? args(kv_append_rope<false>) : args(kv_append_rope<true>);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_page_copy(const Geometry& g, const PlanView& p, void* kpool, void* vpool, cudaStream_t st) {
   if (p.n_copies == 0) return cudaSuccess;
   dim3 grid(p.n_copies * g.num_layers, 2);
-  page_copy<<<grid, 256, 0, st>>>(g, p, static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool));
-  return cudaGetLastError();
+  const cudaError_t e =
+      launch_pdl(page_copy, grid, 256, 0, st, g, p, static_cast<uint8_t*>(kpool), static_cast<uint8_t*>(vpool));
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pie

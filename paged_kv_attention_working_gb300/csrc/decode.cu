@@ -7,14 +7,15 @@
 // The item's pages stream through a ring of shared-memory stages, one 1-D
 // bulk async copy per K and per V page block (the pool's block layout is
 // already bank-conflict free for ldmatrix, see pie_attn.h), filled by a
-// producer warp.  Four consumer warps run QK^T and PV on the tensor cores
-// with warp-level m16n8k16 MMA (M = 16 query heads x rows, N = 8 keys or 8
-// head-dim columns) and keep an online softmax in registers.  When the item
-// has a single 16-row M tile the four warps take alternate pages and merge
-// their softmax states at the end; with 2 or 4 M tiles each warp owns a
-// tile and every page is read from HBM once for all of them, which is what
-// makes a fork group's shared pages cost one read per group ("How Pie
-// thinks", section 4: the prompt is computed once and shared).
+// producer warp.  Four consumer warps run the products on the tensor cores
+// with warp-level m16n8k16 MMA, keys and head dims on the MMA's 16-wide M
+// side and the item's rows x heads on its 8-wide N side (S^T = K Q^T, O^T
+// += V^T P^T), and keep an online softmax per column in registers.  With a
+// single N tile the four warps take alternate pages and merge their softmax
+// states at the end; with more, each warp owns one or two N tiles and every
+// page is read from HBM once for all of them, which is what makes a fork
+// group's shared pages cost one read per group ("How Pie thinks", section
+// 4: the prompt is computed once and shared).
 //
 // E4M3 pages are converted in registers to f16 (exact) and the per-head
 // scales are folded into the softmax and output scaling.  With a logit soft
@@ -28,7 +29,7 @@
 #include <type_traits>
 
 #include "../../include/pie_attn.h"
-#include "func_attr.h"
+#include "launch.h"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -38,20 +39,25 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
-template <bool E4M3, int D>
+template <bool E4M3, int D, int NTW>
 struct DecodeCfg {
   static constexpr int kEsize = E4M3 ? 1 : 2;
   static constexpr int kBlock = kPageSize * D * kEsize;  // bytes per page-head block
   static constexpr int kStages = E4M3 ? 12 : 8;
   static constexpr int kStageBytes = 2 * kBlock;
-  static constexpr int kNT = D / 8;  // n-tiles of the output (head dim)
-  static constexpr int kKS = D / 16; // k-steps of QK^T
-  static constexpr int kCombineFloats = kConsumerWarps * 32 * (kNT * 4 + 4);
+  static constexpr int kNTW = NTW;   // N tiles (8 rows x heads each) per warp at most
+  static constexpr int kMT = D / 16; // M tiles of the head dim in O^T
+  static constexpr int kKS = D / 16; // k-steps of S^T
+  // per thread: O^T fragments and (max, max, sum, sum) per N tile; the
+  // float4 stride is odd, so 8 lanes' float4 stores hit 8 bank groups
+  static constexpr int kCombineBase = kNTW * kMT * 4 + kNTW * 4;
+  static constexpr int kCombineStride = (kCombineBase / 4) % 2 ? kCombineBase : kCombineBase + 4;
+  static constexpr int kCombineFloats = kConsumerWarps * 32 * kCombineStride;
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kSmem = (kRing > kCombineFloats * 4 ? kRing : kCombineFloats * 4) + 2 * kStages * 8 + 16;
 };
 
-template <bool E4M3, int D, bool CAP>
+template <bool E4M3, int D, bool CAP, int NTW>
 __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanView p, int layer,
                                                           const __nv_bfloat16* __restrict__ q,
                                                           const uint8_t* __restrict__ kpool,
@@ -61,7 +67,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                                                           float* __restrict__ part_acc, float* __restrict__ part_ml,
                                                           int* err) {
-  using C = DecodeCfg<E4M3, D>;
+  using C = DecodeCfg<E4M3, D, NTW>;
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (C::kSmem - 2 * C::kStages * 8 - 16));
   uint64_t* empty = full + C::kStages;
@@ -70,15 +78,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
   const int head = blockIdx.y;
   const int G = g.hq / g.hkv;
   const int M = it.n_rows * G;
-  const int n_mt = M <= 16 ? 1 : (M <= 32 ? 2 : 4);
-  const int n_grp = kConsumerWarps / n_mt;
+  // N tiles of 8 rows x heads; owner warps hold two each and read every page
+  // of the item, the others take alternate pages (n_grp groups)
+  const int n_nt = (M + 7) >> 3;
+  const int n_own = n_nt <= C::kNTW ? 1 : (n_nt <= 2 * C::kNTW ? 2 : 4);  // n_nt <= 4 * kNTW
+  const int n_grp = kConsumerWarps / n_own;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t layer_blk = (static_cast<int64_t>(layer) * g.num_pages) * g.hkv;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], n_mt);
+      mbar_init(&empty[s], n_own);
     }
     fence_mbar_init();
   }
@@ -109,8 +120,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
   }
 
   // -------------------------------------------------------------- consumers
-  const int mt = warp % n_mt, grp = warp / n_mt;
-  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group / thread in quad
+  // Keys and head dims are the MMA's M side, the item's rows x query heads
+  // its N side: S^T = K Q^T (M = 16 keys, N = 8 columns, K = head dim) and
+  // O^T += V^T P^T (M = 16 dims, N = 8 columns, K = 16 keys).  A decode row
+  // of 4 or 8 query heads then fills half or all of an 8-wide N tile instead
+  // of a quarter or half of a 16-row M tile, which halves the MMAs and the
+  // softmax work per page.  Thread (g = lane / 4, t = lane % 4) holds, per
+  // N tile, the scores of keys g and g + 8 for columns 2t and 2t + 1, and
+  // the B fragment of Q^T for column g.
+  const int ow = warp % n_own, grp = warp / n_own;
+  const int ntw = max(0, min(C::kNTW, n_nt - C::kNTW * ow));  // N tiles of this warp
+  const int gq = lane >> 2, tq = lane & 3;
   const float kdq = E4M3 ? kscale[layer * g.hkv + head] : 1.0f;
   const float vdq = E4M3 ? vscale[layer * g.hkv + head] : 1.0f;
   // scores in log2 units: s * qk_scale, or with the soft cap c,
@@ -119,215 +139,254 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
   const float cap_pre = CAP ? kdq * rsqrtf(static_cast<float>(D)) / g.softcap : 0.f;
   const float cap_post = CAP ? g.softcap * 1.4426950408889634f : 0.f;
 
-  // the two M rows this thread holds: m = 16*mt + gq (+8)
-  int mrow[2], mpos[2];
-  const __nv_bfloat16* qptr[2];
-  for (int h = 0; h < 2; ++h) {
-    int m = 16 * mt + gq + 8 * h;
-    mrow[h] = -1;
-    mpos[h] = -1;
-    qptr[h] = nullptr;
-    if (m < M) {
-      int rl = m / G, hl = m % G;
-      int row = p.row_list[it.rows_off + rl];
-      mrow[h] = row;
-      mpos[h] = p.row_pos[row];
-      qptr[h] = q + (static_cast<int64_t>(row) * g.hq + head * G + hl) * D;
-    }
-  }
-  // Q as A fragments: qa[ks][0..3] = (row g, k 2t..) (row g+8, k 2t..) (row g, k 2t+8..) (row g+8, k 2t+8..)
-  uint32_t qa[C::kKS][4];
+  // Q^T as B fragments: qb[i][ks] = (k 2t, 2t+1 ; column g) (k 2t+8, 2t+9 ;
+  // column g).  e4m3: k slots 2t, 2t+1, 2t+8, 2t+9 of a 16-dim step are dims
+  // 4t .. 4t+3 (the order the e4m3 K bytes arrive in; the sum over k is the
+  // same).  colpos[i][e]: position of the row of column 2t + e (-1 = none).
+  uint32_t qb[C::kNTW][C::kKS][2];
+  int colpos[C::kNTW][2];
 #pragma unroll
-  for (int ks = 0; ks < C::kKS; ++ks) {
+  for (int i = 0; i < C::kNTW; ++i) {
+    const int mq = 8 * (C::kNTW * ow + i) + gq;
+    const __nv_bfloat16* qp = nullptr;
+    if (i < ntw && mq < M)
+      qp = q + (static_cast<int64_t>(p.row_list[it.rows_off + mq / G]) * g.hq + head * G + mq % G) * D;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t lo = 0, hi = 0;
-      if (qptr[h]) {
+    for (int ks = 0; ks < C::kKS; ++ks) {
+      uint32_t b0 = 0, b1 = 0;
+      if (qp) {
         if constexpr (!E4M3) {
-          lo = *reinterpret_cast<const uint32_t*>(qptr[h] + 16 * ks + 2 * tq);
-          hi = *reinterpret_cast<const uint32_t*>(qptr[h] + 16 * ks + 8 + 2 * tq);
+          b0 = *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * tq);
+          b1 = *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * tq);
         } else {
-          // k-slots 2t,2t+1 <-> d 16ks+4t, +1 ; 2t+8,2t+9 <-> d 16ks+4t+2, +3
-          uint2 w = *reinterpret_cast<const uint2*>(qptr[h] + 16 * ks + 4 * tq);
-          float f0 = __uint_as_float(w.x << 16), f1 = __uint_as_float(w.x & 0xFFFF0000u);
-          float f2 = __uint_as_float(w.y << 16), f3 = __uint_as_float(w.y & 0xFFFF0000u);
-          lo = pack_f16(f0, f1);
-          hi = pack_f16(f2, f3);
+          const uint2 w = *reinterpret_cast<const uint2*>(qp + 16 * ks + 4 * tq);
+          b0 = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+          b1 = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
         }
       }
-      qa[ks][h] = lo;
-      qa[ks][2 + h] = hi;
+      qb[i][ks][0] = b0;
+      qb[i][ks][1] = b1;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int m = 8 * (C::kNTW * ow + i) + 2 * tq + e;
+      colpos[i][e] = i < ntw && m < M ? p.row_pos[p.row_list[it.rows_off + m / G]] : -1;
     }
   }
 
-  float o[C::kNT][4];
+  // O^T accumulators: o[i][mt] = (dim row g, columns 2t, 2t+1), (dim row
+  // g + 8, columns 2t, 2t+1) of M tile mt; bf16 rows are dims 16mt + g and
+  // 16mt + g + 8, e4m3 rows dims 16mt + 2g and 16mt + 2g + 1.
+  float o[C::kNTW][C::kMT][4];
 #pragma unroll
-  for (int i = 0; i < C::kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float mx[2] = {-INFINITY, -INFINITY}, sum[2] = {0.f, 0.f};
+  for (int i = 0; i < C::kNTW; ++i)
+#pragma unroll
+    for (int mt = 0; mt < C::kMT; ++mt) o[i][mt][0] = o[i][mt][1] = o[i][mt][2] = o[i][mt][3] = 0.f;
+  // per column: the running reference max (log2 units) and this thread's
+  // share of the row sum (keys g and g + 8 of every page it saw)
+  float mx[C::kNTW][2], sum[C::kNTW][2];
+#pragma unroll
+  for (int i = 0; i < C::kNTW; ++i) mx[i][0] = mx[i][1] = -INFINITY, sum[i][0] = sum[i][1] = 0.f;
 
   for (int j = grp; j < it.n_pages; j += n_grp) {
     const int s = j % C::kStages;
     // warp-uniform: the shuffles and MMAs below need every lane
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / C::kStages) & 1, err))) break;
-    const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
-    const uint32_t vb = kb + C::kBlock;
+    if (ntw > 0) {
+      const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
+      const uint32_t vb = kb + C::kBlock;
 
-    // ---- S = Q K^T for 16 keys: two n-tiles of 8 keys
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if constexpr (!E4M3) {
-      const int key = (lane & 7) + ((lane >> 4) << 3);
-      const int csel = (lane >> 3) & 1;
+      // ---- S^T = K Q^T: A = K (16 keys x 16 dims per step) by ldmatrix:
+      // matrices (keys 0-7, low chunk) (keys 8-15, low) (keys 0-7, high) (keys 8-15, high)
+      float sc[C::kNTW][4];
 #pragma unroll
-      for (int ks = 0; ks < C::kKS; ++ks) {
-        int panel = ks >> 2, c = 2 * (ks & 3) + csel;
-        uint32_t addr = kb + panel * 2048 + key * 128 + 16 * (c ^ (key & 7));
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(addr, b0, b1, b2, b3);
-        mma16816<true>(sc[0], qa[ks], b0, b1);
-        mma16816<true>(sc[1], qa[ks], b2, b3);
-      }
-    } else {
-      const int key = (lane & 7) + ((lane >> 4) << 3);
-      const int csel = (lane >> 3) & 1;
-#pragma unroll
-      for (int kp = 0; kp < C::kKS / 2; ++kp) {
-        int c = 2 * kp + csel;
-        uint32_t addr = kb + key * 128 + 16 * (c ^ (key & 7));
-        uint32_t r0, r1, r2, r3;  // (keys 0-7, chunk 2kp) (0-7, 2kp+1) (8-15, 2kp) (8-15, 2kp+1)
-        ldsm_x4(addr, r0, r1, r2, r3);
-        // bytes 4t, 4t+1 -> k-slots 2t, 2t+1; bytes 4t+2, 4t+3 -> k-slots 2t+8, 2t+9
-        mma16816<false>(sc[0], qa[2 * kp], e4m3x2_lo_to_f16x2(r0), e4m3x2_hi_to_f16x2(r0));
-        mma16816<false>(sc[1], qa[2 * kp], e4m3x2_lo_to_f16x2(r2), e4m3x2_hi_to_f16x2(r2));
-        mma16816<false>(sc[0], qa[2 * kp + 1], e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r1));
-        mma16816<false>(sc[1], qa[2 * kp + 1], e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r3));
-      }
-    }
-
-    // ---- mask, online softmax (log2 domain)
-    const int kbase = it.key_base + 16 * j;
-    float pm[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float best = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          int kpos = kbase + nt * 8 + 2 * tq + e;
-          float v;
-          if constexpr (CAP)
-            v = kpos <= mpos[h] ? tanh_approx(sc[nt][2 * h + e] * cap_pre) * cap_post : -INFINITY;
-          else
-            v = kpos <= mpos[h] ? sc[nt][2 * h + e] * qk_scale : -INFINITY;
-          sc[nt][2 * h + e] = v;
-          best = fmaxf(best, v);
-        }
-      best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 1));
-      best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 2));
-      // The reference max only moves when the row max exceeds it by more
-      // than 8 (log2 units): weights stay <= 2^8, and O is rescaled rarely.
-      const bool up = best > mx[h] + 8.f;
-      const float mnew = up ? best : mx[h];
-      const float base = mnew == -INFINITY ? 0.f : mnew;
-      pm[h] = base;
-      if (__any_sync(0xffffffffu, up)) {
-        const float alpha = up ? ex2(mx[h] - base) : 1.f;
-        sum[h] *= alpha;
-#pragma unroll
-        for (int i = 0; i < C::kNT; ++i) {
-          o[i][2 * h] *= alpha;
-          o[i][2 * h + 1] *= alpha;
-        }
-      }
-      mx[h] = mnew;
-    }
-    uint32_t pa[4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float e0 = ex2(sc[nt][2 * h] - pm[h]), e1 = ex2(sc[nt][2 * h + 1] - pm[h]);
-        sum[h] += e0 + e1;
-        pa[2 * nt + h] = E4M3 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-      }
-
-    // ---- O += P V
-    if constexpr (!E4M3) {
+      for (int i = 0; i < C::kNTW; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
       const int key = (lane & 7) + (((lane >> 3) & 1) << 3);
       const int csel = lane >> 4;
+      if constexpr (!E4M3) {
 #pragma unroll
-      for (int np = 0; np < C::kNT / 2; ++np) {
-        int cc = 2 * np + csel;  // 16-byte d chunk (8 columns)
-        int panel = cc >> 3, c = cc & 7;
-        uint32_t addr = vb + panel * 2048 + key * 128 + 16 * (c ^ (key & 7));
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma16816<true>(o[2 * np], pa, b0, b1);
-        mma16816<true>(o[2 * np + 1], pa, b2, b3);
+        for (int ks = 0; ks < C::kKS; ++ks) {
+          const int c = 2 * (ks & 3) + csel;
+          uint32_t a[4];
+          ldsm_x4(kb + (ks >> 2) * 2048 + key * 128 + 16 * (c ^ (key & 7)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int i = 0; i < C::kNTW; ++i)
+            if (i < ntw) mma16816<true>(sc[i], a, qb[i][ks][0], qb[i][ks][1]);
+        }
+      } else {
+        // e4m3 bytes: (keys 0-7, chunk 2kp) (keys 8-15, 2kp) (keys 0-7, 2kp+1)
+        // (keys 8-15, 2kp+1); a lane's 4 bytes are dims 4t .. 4t+3 of its key
+#pragma unroll
+        for (int kp = 0; kp < C::kKS / 2; ++kp) {
+          const int c = 2 * kp + csel;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kb + key * 128 + 16 * (c ^ (key & 7)), r0, r1, r2, r3);
+          const uint32_t a0[4] = {e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
+                                  e4m3x2_hi_to_f16x2(r1)};
+          const uint32_t a1[4] = {e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
+                                  e4m3x2_hi_to_f16x2(r3)};
+#pragma unroll
+          for (int i = 0; i < C::kNTW; ++i)
+            if (i < ntw) {
+              mma16816<false>(sc[i], a0, qb[i][2 * kp][0], qb[i][2 * kp][1]);
+              mma16816<false>(sc[i], a1, qb[i][2 * kp + 1][0], qb[i][2 * kp + 1][1]);
+            }
+        }
       }
-    } else {
-      // Transposing loads of 16-bit units (two e4m3 dims): matrices (keys
-      // 0-7, chunk 2cp), (keys 8-15, 2cp), (0-7, 2cp+1), (8-15, 2cp+1); each
-      // register holds (key 2t: dims 2g, 2g+1) (key 2t+1: dims 2g, 2g+1),
-      // and one byte permute pairs the keys per dim.  n-tile 2c takes dims
-      // 16c + 2n, n-tile 2c+1 dims 16c + 2n + 1 (undone when writing out).
-      const int vkey = (lane & 7) + (((lane >> 3) & 1) << 3);
-      const int vsel = lane >> 4;
+
+      // ---- mask, online softmax per column (log2 domain); P^T to B fragments
+      const int kpos0 = it.key_base + 16 * j + gq, kpos1 = kpos0 + 8;
+      uint32_t pb[C::kNTW][2];
 #pragma unroll
-      for (int cp = 0; cp < D / 32; ++cp) {
-        const int c = 2 * cp + vsel;
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(vb + vkey * 128 + 16 * (c ^ (vkey & 7)), r0, r1, r2, r3);
-        const uint32_t x0 = prmt(r0, r0, 0x3120), x1 = prmt(r1, r1, 0x3120);
-        const uint32_t x2 = prmt(r2, r2, 0x3120), x3 = prmt(r3, r3, 0x3120);
-        mma16816<false>(o[4 * cp], pa, e4m3x2_lo_to_f16x2(x0), e4m3x2_lo_to_f16x2(x1));
-        mma16816<false>(o[4 * cp + 1], pa, e4m3x2_hi_to_f16x2(x0), e4m3x2_hi_to_f16x2(x1));
-        mma16816<false>(o[4 * cp + 2], pa, e4m3x2_lo_to_f16x2(x2), e4m3x2_lo_to_f16x2(x3));
-        mma16816<false>(o[4 * cp + 3], pa, e4m3x2_hi_to_f16x2(x2), e4m3x2_hi_to_f16x2(x3));
+      for (int i = 0; i < C::kNTW; ++i) {
+        if (i >= ntw) break;
+        float v[2][2];  // [column e][key g, g + 8]
+        bool grow = false;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if constexpr (CAP) {
+            v[e][0] = kpos0 <= colpos[i][e] ? tanh_approx(sc[i][e] * cap_pre) * cap_post : -INFINITY;
+            v[e][1] = kpos1 <= colpos[i][e] ? tanh_approx(sc[i][2 + e] * cap_pre) * cap_post : -INFINITY;
+          } else {
+            v[e][0] = kpos0 <= colpos[i][e] ? sc[i][e] * qk_scale : -INFINITY;
+            v[e][1] = kpos1 <= colpos[i][e] ? sc[i][2 + e] * qk_scale : -INFINITY;
+          }
+          grow |= fmaxf(v[e][0], v[e][1]) > mx[i][e] + 8.f;
+        }
+        // The reference max of a column only moves when one of its scores
+        // exceeds it by more than 8 (log2 units): weights stay <= 2^8 and the
+        // column's 8 lanes must agree on it, so the cross-lane max is taken
+        // only then (after the first page, rarely).
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float best = fmaxf(v[e][0], v[e][1]);
+            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 4));
+            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 8));
+            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 16));
+            if (best > mx[i][e] + 8.f) {
+              const float alpha = mx[i][e] == -INFINITY ? 0.f : ex2(mx[i][e] - best);
+              sum[i][e] *= alpha;
+#pragma unroll
+              for (int mt = 0; mt < C::kMT; ++mt) {
+                o[i][mt][e] *= alpha;
+                o[i][mt][2 + e] *= alpha;
+              }
+              mx[i][e] = best;
+            }
+          }
+        }
+        float w[2][2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float base = mx[i][e] == -INFINITY ? 0.f : mx[i][e];
+          w[e][0] = ex2(v[e][0] - base);
+          w[e][1] = ex2(v[e][1] - base);
+          sum[i][e] += w[e][0] + w[e][1];
+        }
+        // (key g: columns 2t, 2t+1) and (key g + 8: ...) are 8x8 blocks in
+        // the layout ldmatrix gives; transposed they are the B fragment
+        // (keys 2t, 2t+1 ; column g) and (keys 2t+8, 2t+9 ; column g)
+        pb[i][0] = movmatrix_t(E4M3 ? pack_f16(w[0][0], w[1][0]) : pack_bf16(w[0][0], w[1][0]));
+        pb[i][1] = movmatrix_t(E4M3 ? pack_f16(w[0][1], w[1][1]) : pack_bf16(w[0][1], w[1][1]));
+      }
+
+      // ---- O^T += V^T P^T: A = V^T (16 dims x 16 keys) by transposing ldmatrix
+      if constexpr (!E4M3) {
+        // matrices (keys 0-7, dims 16mt..+7) (keys 0-7, +8..+15) (keys 8-15, ..) (keys 8-15, ..)
+        const int vkey = (lane & 7) + ((lane >> 4) << 3);
+        const int vch = (lane >> 3) & 1;
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt) {
+          const int c = 2 * (mt & 3) + vch;
+          uint32_t a[4];
+          ldsm_x4_t(vb + (mt >> 2) * 2048 + vkey * 128 + 16 * (c ^ (vkey & 7)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int i = 0; i < C::kNTW; ++i)
+            if (i < ntw) mma16816<true>(o[i][mt], a, pb[i][0], pb[i][1]);
+        }
+      } else {
+        // 16-bit units of two e4m3 dims: matrices (keys 0-7, chunk 2cp) (keys
+        // 8-15, 2cp) (keys 0-7, 2cp+1) (keys 8-15, 2cp+1); a lane gets (key 2t:
+        // dims 2g, 2g+1) (key 2t+1: dims 2g, 2g+1) and one byte permute pairs
+        // the keys per dim: M rows g and g + 8 are dims 2g and 2g + 1
+        const int vkey = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int vsel = lane >> 4;
+#pragma unroll
+        for (int cp = 0; cp < D / 32; ++cp) {
+          const int c = 2 * cp + vsel;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vb + vkey * 128 + 16 * (c ^ (vkey & 7)), r0, r1, r2, r3);
+          const uint32_t x0 = prmt(r0, r0, 0x3120), x1 = prmt(r1, r1, 0x3120);
+          const uint32_t x2 = prmt(r2, r2, 0x3120), x3 = prmt(r3, r3, 0x3120);
+          const uint32_t a0[4] = {e4m3x2_lo_to_f16x2(x0), e4m3x2_hi_to_f16x2(x0), e4m3x2_lo_to_f16x2(x1),
+                                  e4m3x2_hi_to_f16x2(x1)};
+          const uint32_t a1[4] = {e4m3x2_lo_to_f16x2(x2), e4m3x2_hi_to_f16x2(x2), e4m3x2_lo_to_f16x2(x3),
+                                  e4m3x2_hi_to_f16x2(x3)};
+#pragma unroll
+          for (int i = 0; i < C::kNTW; ++i)
+            if (i < ntw) {
+              mma16816<false>(o[i][2 * cp], a0, pb[i][0], pb[i][1]);
+              mma16816<false>(o[i][2 * cp + 1], a1, pb[i][0], pb[i][1]);
+            }
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
 
-  // ---- finish: quad sums, then merge warps that shared an M tile
+  // ---- finish: each column's sum over its 8 lanes, then merge the warps
+  // that took alternate pages of the same columns
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
-    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
-  }
+  for (int i = 0; i < C::kNTW; ++i)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      sum[i][e] += __shfl_xor_sync(0xffffffffu, sum[i][e], 4);
+      sum[i][e] += __shfl_xor_sync(0xffffffffu, sum[i][e], 8);
+      sum[i][e] += __shfl_xor_sync(0xffffffffu, sum[i][e], 16);
+    }
   if (n_grp > 1) {
     __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32));
     float* cm = reinterpret_cast<float*>(smem);
-    const int stride = C::kNT * 4 + 4;
-    float* mine = cm + (warp * 32 + lane) * stride;
+    float* mine = cm + (warp * 32 + lane) * C::kCombineStride;
     if (grp > 0) {
 #pragma unroll
-      for (int i = 0; i < C::kNT; ++i)
+      for (int i = 0; i < C::kNTW; ++i) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) mine[i * 4 + e] = o[i][e];
-      mine[C::kNT * 4 + 0] = mx[0];
-      mine[C::kNT * 4 + 1] = mx[1];
-      mine[C::kNT * 4 + 2] = sum[0];
-      mine[C::kNT * 4 + 3] = sum[1];
+        for (int mt = 0; mt < C::kMT; ++mt)
+          *reinterpret_cast<float4*>(mine + (i * C::kMT + mt) * 4) =
+              make_float4(o[i][mt][0], o[i][mt][1], o[i][mt][2], o[i][mt][3]);
+        *reinterpret_cast<float4*>(mine + (C::kNTW * C::kMT + i) * 4) =
+            make_float4(mx[i][0], mx[i][1], sum[i][0], sum[i][1]);
+      }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32));
     if (grp > 0) return;
     for (int og = 1; og < n_grp; ++og) {
-      const float* th = cm + ((og * n_mt + mt) * 32 + lane) * stride;
+      const float* th = cm + ((og * n_own + ow) * 32 + lane) * C::kCombineStride;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float m2 = th[C::kNT * 4 + h], l2 = th[C::kNT * 4 + 2 + h];
-        float mnew = fmaxf(mx[h], m2);
-        float base = mnew == -INFINITY ? 0.f : mnew;
-        float a1 = ex2(mx[h] - base), a2 = ex2(m2 - base);
-        sum[h] = sum[h] * a1 + l2 * a2;
-        mx[h] = mnew;
+      for (int i = 0; i < C::kNTW; ++i) {
+        const float4 st = *reinterpret_cast<const float4*>(th + (C::kNTW * C::kMT + i) * 4);
+        const float m2[2] = {st.x, st.y}, l2[2] = {st.z, st.w};
+        float a1[2], a2[2];
 #pragma unroll
-        for (int i = 0; i < C::kNT; ++i) {
-          o[i][2 * h] = o[i][2 * h] * a1 + th[i * 4 + 2 * h] * a2;
-          o[i][2 * h + 1] = o[i][2 * h + 1] * a1 + th[i * 4 + 2 * h + 1] * a2;
+        for (int e = 0; e < 2; ++e) {
+          const float mnew = fmaxf(mx[i][e], m2[e]);
+          const float base = mnew == -INFINITY ? 0.f : mnew;
+          a1[e] = ex2(mx[i][e] - base);
+          a2[e] = ex2(m2[e] - base);
+          sum[i][e] = sum[i][e] * a1[e] + l2[e] * a2[e];
+          mx[i][e] = mnew;
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt) {
+          const float4 v = *reinterpret_cast<const float4*>(th + (i * C::kMT + mt) * 4);
+          o[i][mt][0] = o[i][mt][0] * a1[0] + v.x * a2[0];
+          o[i][mt][1] = o[i][mt][1] * a1[1] + v.y * a2[1];
+          o[i][mt][2] = o[i][mt][2] * a1[0] + v.z * a2[0];
+          o[i][mt][3] = o[i][mt][3] * a1[1] + v.w * a2[1];
         }
       }
     }
@@ -335,42 +394,71 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanVie
 
   // ---- write: direct bf16 output, or fp32 partial (acc, m, l) for merging
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if (mrow[h] < 0) continue;
-    int m = 16 * mt + gq + 8 * h;
-    int qh = head * G + m % G;
-    int row = mrow[h];
+  for (int i = 0; i < C::kNTW; ++i) {
+    if (i >= ntw) break;
+    const int nt = C::kNTW * ow + i;
+    int colrow[2], colqh[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int m = 8 * nt + 2 * tq + e;
+      colrow[e] = m < M ? p.row_list[it.rows_off + m / G] : -1;
+      colqh[e] = head * G + m % G;
+    }
     if (it.part < 0) {
-      float inv = sum[h] > 0.f ? vdq / sum[h] : 0.f;
-      __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D;
+      float inv[2];
 #pragma unroll
-      for (int i = 0; i < C::kNT; ++i) {
-        if constexpr (!E4M3) {
-          *reinterpret_cast<uint32_t*>(dst + 8 * i + 2 * tq) =
-              pack_bf16(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
-        } else if ((i & 1) == 0) {
-          // n-tiles i (even dims) and i+1 (odd dims) of chunk i/2: dims
-          // 8i + 4t .. 8i + 4t + 3
-          uint2 wv;
-          wv.x = pack_bf16(o[i][2 * h] * inv, o[i + 1][2 * h] * inv);
-          wv.y = pack_bf16(o[i][2 * h + 1] * inv, o[i + 1][2 * h + 1] * inv);
-          *reinterpret_cast<uint2*>(dst + 8 * i + 4 * tq) = wv;
+      for (int e = 0; e < 2; ++e) inv[e] = sum[i][e] > 0.f ? vdq / sum[i][e] : 0.f;
+      if constexpr (!E4M3) {
+        // transpose (dim g: columns 2t, 2t+1) blocks to (column g: dims 2t,
+        // 2t+1): each lane then stores whole bf16 pairs of one head
+        const int m = 8 * nt + gq;
+        __nv_bfloat16* dst =
+            m < M ? out + (static_cast<int64_t>(p.row_list[it.rows_off + m / G]) * g.hq + head * G + m % G) * D
+                  : nullptr;
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt) {
+          const uint32_t lo = movmatrix_t(pack_bf16(o[i][mt][0] * inv[0], o[i][mt][1] * inv[1]));
+          const uint32_t hi = movmatrix_t(pack_bf16(o[i][mt][2] * inv[0], o[i][mt][3] * inv[1]));
+          if (dst) {
+            *reinterpret_cast<uint32_t*>(dst + 16 * mt + 2 * tq) = lo;
+            *reinterpret_cast<uint32_t*>(dst + 16 * mt + 8 + 2 * tq) = hi;
+          }
+        }
+      } else {
+        // rows g and g + 8 of M tile mt are dims 16mt + 2g and 16mt + 2g + 1
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (colrow[e] < 0) continue;
+          __nv_bfloat16* dst = out + (static_cast<int64_t>(colrow[e]) * g.hq + colqh[e]) * D;
+#pragma unroll
+          for (int mt = 0; mt < C::kMT; ++mt)
+            *reinterpret_cast<uint32_t*>(dst + 16 * mt + 2 * gq) =
+                pack_bf16(o[i][mt][e] * inv[e], o[i][mt][2 + e] * inv[e]);
         }
       }
-      if (lse && tq == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (mx[h] + __log2f(sum[h])) * 0.6931471805599453f;
+      if (lse && gq == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (colrow[e] >= 0)
+            lse[static_cast<int64_t>(colrow[e]) * g.hq + colqh[e]] = (mx[i][e] + __log2f(sum[i][e])) * 0.6931471805599453f;
+      }
     } else {
-      int64_t slot = static_cast<int64_t>(p.row_part_base[row] + it.part) * g.hq + qh;
-      float* dst = part_acc + slot * D;
 #pragma unroll
-      for (int i = 0; i < C::kNT; ++i) {
-        if constexpr (!E4M3) {
-          *reinterpret_cast<float2*>(dst + 8 * i + 2 * tq) = make_float2(o[i][2 * h] * vdq, o[i][2 * h + 1] * vdq);
-        } else if ((i & 1) == 0) {
-          *reinterpret_cast<float4*>(dst + 8 * i + 4 * tq) =
-              make_float4(o[i][2 * h] * vdq, o[i + 1][2 * h] * vdq, o[i][2 * h + 1] * vdq, o[i + 1][2 * h + 1] * vdq);
+      for (int e = 0; e < 2; ++e) {
+        if (colrow[e] < 0) continue;
+        const int64_t slot = static_cast<int64_t>(p.row_part_base[colrow[e]] + it.part) * g.hq + colqh[e];
+        float* dst = part_acc + slot * D;
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt) {
+          if constexpr (!E4M3) {
+            dst[16 * mt + gq] = o[i][mt][e] * vdq;
+            dst[16 * mt + 8 + gq] = o[i][mt][2 + e] * vdq;
+          } else {
+            *reinterpret_cast<float2*>(dst + 16 * mt + 2 * gq) = make_float2(o[i][mt][e] * vdq, o[i][mt][2 + e] * vdq);
+          }
         }
+        if (gq == 0) *reinterpret_cast<float2*>(part_ml + slot * 2) = make_float2(mx[i][e], sum[i][e]);
       }
-      if (tq == 0) *reinterpret_cast<float2*>(part_ml + slot * 2) = make_float2(mx[h], sum[h]);
     }
   }
 }
@@ -385,6 +473,8 @@ __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__
   // (32 parts at a time), so the parts' loads are issued together; the
   // weights reach every lane by shuffle, and each lane accumulates E dims of
   // the parts' partial outputs with vector loads, four parts in flight.
+  pdl_wait();
+  pdl_trigger();
   int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.n_merge * g.hq) return;
   int i = wid / g.hq, qh = wid % g.hq;
@@ -438,18 +528,29 @@ __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__
   if (lse && lane == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (m + __log2f(l)) * 0.6931471805599453f;
 }
 
-template <bool E4M3, int D, bool CAP = false>
+template <bool E4M3, int D, bool CAP, int NTW>
 cudaError_t launch_decode_t(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
                             const void* vpool, const float* ks, const float* vs, void* out, float* lse,
                             float* acc, float* ml, int* err, cudaStream_t st) {
-  using C = DecodeCfg<E4M3, D>;
-  cudaError_t e = ensure_smem_attr<decode_kernel<E4M3, D, CAP>>(C::kSmem);
+  using C = DecodeCfg<E4M3, D, NTW>;
+  cudaError_t e = ensure_smem_attr<decode_kernel<E4M3, D, CAP, NTW>>(C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_dec, g.hkv);
-  decode_kernel<E4M3, D, CAP><<<grid, kThreads, C::kSmem, st>>>(
-      g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
-      static_cast<const uint8_t*>(vpool), ks, vs, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
-  return cudaGetLastError();
+  e = launch_pdl(decode_kernel<E4M3, D, CAP, NTW>, grid, kThreads, C::kSmem, st, g, p, layer,
+                 static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
+                 static_cast<const uint8_t*>(vpool), ks, vs, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Items of up to 32 rows x heads take one N tile per warp (fewer registers);
+// a launch with larger items (fork / dedup groups of 33-64) takes two.
+template <bool E4M3, int D, bool CAP>
+cudaError_t launch_decode_n(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
+                            const void* vpool, const float* ks, const float* vs, void* out, float* lse,
+                            float* acc, float* ml, int* err, cudaStream_t st) {
+  return p.max_dec_m > 32
+             ? launch_decode_t<E4M3, D, CAP, 2>(g, p, layer, q, kpool, vpool, ks, vs, out, lse, acc, ml, err, st)
+             : launch_decode_t<E4M3, D, CAP, 1>(g, p, layer, q, kpool, vpool, ks, vs, out, lse, acc, ml, err, st);
 }
 
 }  // namespace
@@ -459,7 +560,7 @@ cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const
                           float* part_acc, float* part_ml, int* err, cudaStream_t st) {
   if (p.n_dec == 0) return cudaSuccess;
 #define PIE_DECODE(E, DD, CP) \
-  launch_decode_t<E, DD, CP>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st)
+  launch_decode_n<E, DD, CP>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st)
   const bool cap = g.softcap > 0.f;
   if (g.kv_dtype == 0 && g.d == 128) return cap ? PIE_DECODE(false, 128, true) : PIE_DECODE(false, 128, false);
   if (g.kv_dtype == 0 && g.d == 64) return cap ? PIE_DECODE(false, 64, true) : PIE_DECODE(false, 64, false);
@@ -489,11 +590,12 @@ cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float*
   if (p.n_merge == 0) return cudaSuccess;
   int64_t warps = static_cast<int64_t>(p.n_merge) * g.hq;
   unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
-  if (g.d == 128)
-    merge_kernel<128><<<blocks, 256, 0, st>>>(g, p, static_cast<__nv_bfloat16*>(out), lse, part_acc, part_ml);
-  else
-    merge_kernel<64><<<blocks, 256, 0, st>>>(g, p, static_cast<__nv_bfloat16*>(out), lse, part_acc, part_ml);
-  return cudaGetLastError();
+  const cudaError_t e =
+      g.d == 128 ? launch_pdl(merge_kernel<128>, blocks, 256, 0, st, g, p, static_cast<__nv_bfloat16*>(out), lse,
+                              part_acc, part_ml)
+                 : launch_pdl(merge_kernel<64>, blocks, 256, 0, st, g, p, static_cast<__nv_bfloat16*>(out), lse,
+                              part_acc, part_ml);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pie
@@ -518,6 +620,8 @@ void* g_noalloc_addr[kMaxDevices] = {};
 __global__ void noalloc_plan(int n_rows, int n_splits, int chunk, int max_pages, const int32_t* __restrict__ seq_lens,
                              WorkItem* items, int32_t* row_pos, int32_t* row_list, int32_t* part_base,
                              int32_t* merge_rows, int32_t* merge_np) {
+  pdl_wait();
+  pdl_trigger();
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_rows * n_splits) return;
   int r = i / n_splits, s = i % n_splits;
@@ -627,9 +731,10 @@ extern "C" pie_status pie_attend_decode_noalloc(const pie_decode_args* a) {
   float* ml = reinterpret_cast<float*>(sc + lay.ml);
 
   const int n_items = R * S;
-  noalloc_plan<<<(n_items + 255) / 256, 256, 0, st>>>(R, S, chunk, maxp, a->seq_lens, items, row_pos, row_list,
-                                                       part_base, merge_rows, merge_np);
-  if (cudaGetLastError() != cudaSuccess) return PIE_ERR_CUDA;
+  if (launch_pdl(noalloc_plan, (n_items + 255) / 256, 256, 0, st, R, S, chunk, maxp, a->seq_lens, items, row_pos,
+                 row_list, part_base, merge_rows, merge_np) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PIE_ERR_CUDA;
 
   Geometry g{a->num_layers, hq, hkv, d, a->num_pages, 0, static_cast<int64_t>(kPageSize) * d * 2};
   PlanView v{};
@@ -648,10 +753,11 @@ extern "C" pie_status pie_attend_decode_noalloc(const pie_decode_args* a) {
   v.n_pre = 0;
   v.n_merge = S > 1 ? R : 0;
   v.n_copies = 0;
-  cudaError_t e = d == 128 ? launch_decode_t<false, 128>(g, v, a->layer, a->q, a->k_pool, a->v_pool, nullptr, nullptr,
-                                                         a->out, a->lse, acc, ml, nullptr, st)
-                           : launch_decode_t<false, 64>(g, v, a->layer, a->q, a->k_pool, a->v_pool, nullptr, nullptr,
-                                                        a->out, a->lse, acc, ml, nullptr, st);
+  v.max_dec_m = G;
+  cudaError_t e = d == 128 ? launch_decode_n<false, 128, false>(g, v, a->layer, a->q, a->k_pool, a->v_pool, nullptr,
+                                                                nullptr, a->out, a->lse, acc, ml, nullptr, st)
+                           : launch_decode_n<false, 64, false>(g, v, a->layer, a->q, a->k_pool, a->v_pool, nullptr,
+                                                               nullptr, a->out, a->lse, acc, ml, nullptr, st);
   if (e == cudaSuccess && S > 1) e = launch_merge(g, v, a->out, a->lse, acc, ml, st);
   return e == cudaSuccess ? PIE_OK : PIE_ERR_CUDA;
 }

@@ -34,6 +34,11 @@ namespace {
 // item (it tiles 256 of them per CTA); the decode kernel takes up to 64.
 constexpr int kDecodeMaxM = 64;
 constexpr int kPrefillTileM = 256;
+// A shared run (fork / dedup group) of at most this many rows x query heads
+// goes to the decode kernel in row tiles of at most kDecodeMaxM, each tile
+// reading the run's pages (from L2 after the first): the whole pass then
+// stays in one decode launch.  Larger runs take the tensor-core kernel.
+constexpr int kDecodeSharedMaxM = 64;
 constexpr int kMinSplitPages = 16;
 
 struct DedupKey {
@@ -181,7 +186,7 @@ struct PlanBuilder {
 };
 
 struct SegInfo {
-  int32_t seg, n0, n_new, row0, table_off, n_pages, shared_pages, group;
+  int32_t seg, n0, n_new, row0, table_off, n_pages, shared_pages;
 };
 
 void split_pages(int32_t n_pages, int32_t chunk, std::vector<std::pair<int32_t, int32_t>>& out) {
@@ -195,54 +200,95 @@ void split_pages(int32_t n_pages, int32_t chunk, std::vector<std::pair<int32_t, 
   }
 }
 
+// A run of pages [p0, p1) that every member segment's table holds: the
+// shared item of a fork / dedup group, attended once for all members' rows.
+struct SharedRun {
+  std::vector<int32_t> members;  // segment indices
+  int32_t p0, p1;
+};
+
+// Prefix tree over the page tables of the segments that may share: at each
+// depth, segments holding the same physical page there form a group; the
+// group's run extends while all its members hold the same pages, and the
+// group then splits by the page where they part.  A fork of a fork thus
+// shares its parent's pages with all its relatives and its own frozen pages
+// with its siblings only.  Only pages before every member's new tokens (full
+// frozen pages) are shared.  shared_end[i] = pages of segment i covered by
+// runs (its private keys start there).
+void shared_runs(const std::vector<SegInfo>& segs, const std::vector<int32_t>& page_ids,
+                 const std::vector<int32_t>& cand, std::vector<SharedRun>& runs, std::vector<int32_t>& shared_end) {
+  auto page_at = [&](int32_t i, int32_t j) { return page_ids[segs[i].table_off + j]; };
+  auto full = [&](int32_t i) { return segs[i].n0 / kPageSize; };
+  struct Work {
+    std::vector<int32_t> members;
+    int32_t depth;
+  };
+  std::vector<Work> stack{{cand, 0}};
+  std::vector<int32_t> order;
+  std::unordered_map<int32_t, std::vector<int32_t>> by_page;
+  while (!stack.empty()) {
+    Work w = std::move(stack.back());
+    stack.pop_back();
+    // partition by the page at `depth`, in order of first appearance
+    by_page.clear();
+    order.clear();
+    for (int32_t i : w.members) {
+      if (full(i) <= w.depth) {
+        shared_end[i] = w.depth;
+        continue;
+      }
+      auto& v = by_page[page_at(i, w.depth)];
+      if (v.empty()) order.push_back(page_at(i, w.depth));
+      v.push_back(i);
+    }
+    std::vector<Work> next;
+    for (int32_t pg : order) {
+      std::vector<int32_t>& m = by_page[pg];
+      if (m.size() < 2) {
+        shared_end[m[0]] = w.depth;
+        continue;
+      }
+      int32_t lim = INT32_MAX;
+      for (int32_t i : m) lim = std::min(lim, full(i));
+      int32_t L = w.depth + 1;
+      for (; L < lim; ++L) {
+        const int32_t p0 = page_at(m[0], L);
+        bool same = true;
+        for (int32_t i : m) same = same && page_at(i, L) == p0;
+        if (!same) break;
+      }
+      runs.push_back({m, w.depth, L});
+      next.push_back({std::move(m), L});
+    }
+    // depth-first, in order: a segment's runs come out shallowest first
+    for (auto it = next.rbegin(); it != next.rend(); ++it) stack.push_back(std::move(*it));
+  }
+}
+
 void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows, PlanBuilder& pb) {
   const int32_t G = c->geo.hq / c->geo.hkv;
   std::vector<SegInfo> segs = segs_in;
-  // fork / dedup groups: segments whose tables start with the same page
-  std::unordered_map<int32_t, std::vector<int32_t>> by_first;
-  std::vector<int32_t> first_order;
-  // Only decode-like segments (few rows) join a group: a prefill chunk reads
-  // its whole context itself, tile by tile, and sharing would only add
-  // partial results for each of its many rows.
-  for (size_t i = 0; i < segs.size(); ++i) {
-    if (static_cast<int64_t>(segs[i].n_new) * G > kDecodeMaxM) continue;
-    int32_t p0 = pb.page_ids[segs[i].table_off];
-    auto& v = by_first[p0];
-    if (v.empty()) first_order.push_back(p0);
-    v.push_back(static_cast<int32_t>(i));
-  }
-  struct Group {
-    std::vector<int32_t> members;
-    int32_t cp;
-  };
-  std::vector<Group> groups;
-  for (int32_t p0 : first_order) {
-    auto& m = by_first[p0];
-    if (m.size() < 2) continue;
-    int32_t cp = INT32_MAX;
-    for (int32_t i : m) cp = std::min(cp, segs[i].n0 / kPageSize);
-    const int32_t* t0 = &pb.page_ids[segs[m[0]].table_off];
-    for (int32_t j = 0; j < cp; ++j)
-      for (int32_t i : m)
-        if (pb.page_ids[segs[i].table_off + j] != t0[j]) {
-          cp = j;
-          break;
-        }
-    if (cp <= 0) continue;
-    for (int32_t i : m) {
-      segs[i].shared_pages = cp;
-      segs[i].group = static_cast<int32_t>(groups.size());
-    }
-    groups.push_back({m, cp});
-  }
+  // Segments of up to one tensor-core row tile (decode rows, speculative
+  // drafts) share: a long prefill chunk reads its whole context itself,
+  // tile by tile, and sharing would only add partial results for each of
+  // its many rows.
+  std::vector<int32_t> cand;
+  for (size_t i = 0; i < segs.size(); ++i)
+    if (static_cast<int64_t>(segs[i].n_new) * G <= kPrefillTileM) cand.push_back(static_cast<int32_t>(i));
+  std::vector<SharedRun> runs;
+  std::vector<int32_t> shared_end(segs.size(), 0);
+  shared_runs(segs, pb.page_ids, cand, runs, shared_end);
+  for (size_t i = 0; i < segs.size(); ++i) segs[i].shared_pages = shared_end[i];
 
+  auto run_rows = [&](const SharedRun& r) {
+    int64_t rows = 0;
+    for (int32_t i : r.members) rows += segs[i].n_new;
+    return rows;
+  };
   // pages of decode-kernel work, to size the KV splits
   int64_t dec_pages = 0;
-  for (auto& g : groups) {
-    int32_t rows = 0;
-    for (int32_t i : g.members) rows += segs[i].n_new;
-    if (static_cast<int64_t>(rows) * G <= kDecodeMaxM) dec_pages += g.cp;
-  }
+  for (auto& r : runs)
+    if (run_rows(r) * G <= kDecodeSharedMaxM) dec_pages += (r.p1 - r.p0) * cdiv(run_rows(r) * G, kDecodeMaxM);
   for (auto& s : segs)
     if (static_cast<int64_t>(s.n_new) * G <= kDecodeMaxM) dec_pages += s.n_pages - s.shared_pages;
   // KV splits aim at about 8 decode CTAs per SM for bf16 pages and 16 for
@@ -261,51 +307,66 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
   std::vector<Pending> items;
   std::vector<std::pair<int32_t, int32_t>> sp;
 
-  // shared items first: part indices 0..k-1 of every member row
-  std::vector<int32_t> group_parts(groups.size(), 0);
-  for (size_t gi = 0; gi < groups.size(); ++gi) {
-    auto& g = groups[gi];
+  // shared items first: a member row's parts are numbered along its runs,
+  // shallowest first, then its private parts
+  std::vector<int32_t> seg_parts(segs.size(), 0);
+  for (const SharedRun& g : runs) {
     int32_t rows_off = static_cast<int32_t>(pb.row_list.size());
     for (int32_t i : g.members)
       for (int32_t r = 0; r < segs[i].n_new; ++r) pb.row_list.push_back(segs[i].row0 + r);
     int32_t rows = static_cast<int32_t>(pb.row_list.size()) - rows_off;
     const SegInfo& s0 = segs[g.members[0]];
-    bool decode = static_cast<int64_t>(rows) * G <= kDecodeMaxM;
+    const int32_t run = g.p1 - g.p0;
+    bool decode = static_cast<int64_t>(rows) * G <= kDecodeSharedMaxM;
     int32_t kv_chunk = chunk;
-    if (!decode) {
-      // tensor-core items: tile the rows by 256 query heads, split the keys
-      // so the group fills the GPU (each page still read once per row tile)
-      int32_t tiles = cdiv(static_cast<int64_t>(rows) * G, kPrefillTileM);
+    int32_t rt_rows = rows;
+    if (decode) {
+      rt_rows = cdiv(rows, cdiv(static_cast<int64_t>(rows) * G, kDecodeMaxM));
+    } else {
+      // tensor-core items: rows in balanced tiles of at most one 128-row Q
+      // tile (a CTA with one Q tile runs S, softmax and PV of a key tile in
+      // about 2500 cycles, two Q tiles take about 4000: for the short runs
+      // of a shared prefix the shorter chain wins); keys split so the
+      // group's items fill about the SMs, each page still read once per row
+      // tile.  At least 4 key tiles (32 pages) per item: shorter splits add
+      // start-up and partials, and more CTAs than SMs keep the pass's
+      // decode CTAs waiting (fork pass, 4096-token prompt, 32 layers: one
+      // Q tile 0.81 ms, two 0.86 ms; 16-page splits with one Q tile 0.96 ms).
+      int32_t tiles = cdiv(static_cast<int64_t>(rows) * G, kPrefillTileM / 2);
+      rt_rows = cdiv(rows, tiles);
       int64_t want = std::max<int64_t>(1, static_cast<int64_t>(c->num_sms) / (c->geo.hkv * tiles));
-      // at least 4 key tiles (32 pages) per item: shorter splits only add
-      // start-up and partials (fork pass, 4096-token prompt: 8 / 16 / 32 / 64
-      // pages measured 1.45 / 1.45 / 1.39 / 1.65 ms per 32-layer pass)
-      kv_chunk = std::max<int32_t>(32, cdiv(g.cp, want));
+      kv_chunk = std::max<int32_t>(32, cdiv(run, want));
     }
-    split_pages(g.cp, kv_chunk, sp);
-    int32_t rt_rows = decode ? rows : std::max(1, kPrefillTileM / G);
+    split_pages(run, kv_chunk, sp);
+    // every member row takes the run's parts at its own next part indices;
+    // the kernels index parts per row (row_part_base[row] + part), so the
+    // members of one run must agree on the index: they do, because a run's
+    // members share every run before it on their paths
+    const int32_t base_part = seg_parts[g.members[0]];
     for (int32_t r0 = 0; r0 < rows; r0 += rt_rows) {
       int32_t nr = std::min(rt_rows, rows - r0);
       for (size_t j = 0; j < sp.size(); ++j) {
         WorkItem it{};
-        it.pages_off = s0.table_off + sp[j].first;
+        it.pages_off = s0.table_off + g.p0 + sp[j].first;
         it.n_pages = sp[j].second;
-        it.key_base = sp[j].first * kPageSize;
+        it.key_base = (g.p0 + sp[j].first) * kPageSize;
         it.n_keys = sp[j].second * kPageSize;
         it.rows_off = rows_off + r0;
         it.n_rows = nr;
-        it.part = static_cast<int32_t>(j);
+        it.part = base_part + static_cast<int32_t>(j);
         items.push_back({it, decode});
       }
     }
-    group_parts[gi] = static_cast<int32_t>(sp.size());
-    for (int32_t i : g.members)
+    for (int32_t i : g.members) {
+      seg_parts[i] += static_cast<int32_t>(sp.size());
       for (int32_t r = 0; r < segs[i].n_new; ++r) n_parts[segs[i].row0 + r] += static_cast<int32_t>(sp.size());
+    }
   }
 
   // private items of each segment
-  for (auto& s : segs) {
-    int32_t base_part = s.group >= 0 ? group_parts[s.group] : 0;
+  for (size_t si = 0; si < segs.size(); ++si) {
+    const SegInfo& s = segs[si];
+    int32_t base_part = seg_parts[si];
     int32_t priv = s.n_pages - s.shared_pages;
     if (static_cast<int64_t>(s.n_new) * G <= kDecodeMaxM) {
       split_pages(priv, chunk, sp);
@@ -715,7 +776,6 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     si.n0 = n0;
     si.n_new = s.n_new;
     si.row0 = static_cast<int32_t>(b->row_pos.size());
-    si.group = -1;
     for (int32_t t = 0; t < s.n_new; ++t) {
       int32_t pos = n0 + t;
       if (pos % kPageSize == 0) {
@@ -754,6 +814,8 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
   v.n_pre = static_cast<int32_t>(pb.pre.size());
   v.n_merge = static_cast<int32_t>(pb.merge_rows.size());
   v.n_copies = static_cast<int32_t>(pb.copies.size());
+  v.max_dec_m = 0;
+  for (const WorkItem& it : pb.dec) v.max_dec_m = std::max(v.max_dec_m, it.n_rows * (c->geo.hq / c->geo.hkv));
   if (c->fail_next_begin) {
     c->fail_next_begin = false;
     undo_reservation(c, undo);
@@ -894,19 +956,21 @@ pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, vo
   // With both kinds of items, the decode launch goes on the side stream so
   // it can take the SMs the tensor-core launch leaves free (a small pass
   // fills only part of the GPU); the two write disjoint outputs and
-  // partials, and the merge waits for both.
+  // partials, and the merge waits for both.  The tensor-core grid is
+  // submitted first: its CTAs need a whole SM each (224 KB of shared
+  // memory), and decode CTAs spread over the SMs first would keep them out.
   const bool both = v.n_pre && v.n_dec;
   if (both) {
     e = cudaEventRecord(c->fork_ev, c->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->side, c->fork_ev, 0);
   }
+  if (e == cudaSuccess && v.n_pre)
+    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
+                            lse, acc, ml, c->d_err, c->stream);
   if (e == cudaSuccess && v.n_dec)
     e = pie::launch_decode(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
                            lse, acc, ml, c->d_err, both ? c->side : c->stream);
   if (e == cudaSuccess && both) e = cudaEventRecord(c->join_ev, c->side);
-  if (e == cudaSuccess && v.n_pre)
-    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
-                            lse, acc, ml, c->d_err, c->stream);
   if (e == cudaSuccess && both) e = cudaStreamWaitEvent(c->stream, c->join_ev, 0);
   if (e == cudaSuccess && v.n_merge) e = pie::launch_merge(c->geo, v, out, lse, acc, ml, c->stream);
   if (e != cudaSuccess) return cuda_fail(c, e, "attend launch");

@@ -42,6 +42,7 @@ struct PlanView {
   const int32_t* merge_nparts;
   const CopyItem* copies;
   int32_t n_rows, n_dec, n_pre, n_merge, n_copies;
+  int32_t max_dec_m;             // largest rows x query heads of a decode item
 };
 
 struct Geometry {

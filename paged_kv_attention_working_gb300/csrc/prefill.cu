@@ -48,7 +48,7 @@
 
 #include <cmath>
 
-#include "func_attr.h"
+#include "launch.h"
 #include "plan.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_acc,
                    float* __restrict__ part_ml, int* err) {
   using C = PreCfg<D, E4M3>;
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -208,25 +210,6 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
-  // Q tiles -> shared memory, 128-byte swizzled K-major; rows past M are zero
-  {
-    constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    const int total = n_qt * 128 * kChunks;
-    for (int idx = threadIdx.x; idx < total; idx += C::kThreads) {
-      int m = idx / kChunks, c16 = idx % kChunks;
-      int t = m >> 7, r = m & 127;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (m < M) {
-        int row = p.row_list[it.rows_off + m / G];
-        int qh = head * G + m % G;
-        v = *reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(row) * g.hq + qh) * D + c16 * 8);
-        if constexpr (E4M3) v = bf16x8_to_f16x8(v);
-      }
-      int panel = c16 >> 3, c = c16 & 7;
-      *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
-    }
-  }
-  tc::fence_proxy_async_smem();
   if (warp == 8) {
     tc::alloc(tmem_slot, C::kTmemCols);
     tc::relinquish();
@@ -235,6 +218,53 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // Q tiles -> shared memory, 128-byte swizzled K-major, rows past M zero;
+  // loaded by the softmax warps while the producers already fetch K and V.
+  // Every load of a thread is in flight at once (row indices first, then
+  // 16-byte cp.async copies, or register loads for the f16 conversion of
+  // e4m3 contexts); a load loop that waited for each copy in turn cost a
+  // few microseconds per CTA, the whole run time of a short item.  The MMA
+  // thread issues no product before the named barrier below.
+  if (warp < 8) {
+    constexpr int kChunks = D / 8;  // 16-byte chunks per row
+    constexpr int kPer = 2 * 128 * kChunks / 256;
+    const int total = n_qt * 128 * kChunks;
+    int src_row[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = threadIdx.x + 256 * k, m = idx / kChunks;
+      src_row[k] = idx < total && m < M ? p.row_list[it.rows_off + m / G] : -1;
+    }
+    uint4 v[E4M3 ? kPer : 1];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
+      if (src_row[k] >= 0) {
+        const __nv_bfloat16* src = q + (static_cast<int64_t>(src_row[k]) * g.hq + head * G + m % G) * D + c16 * 8;
+        if constexpr (E4M3) {
+          v[k] = *reinterpret_cast<const uint4*>(src);
+        } else {
+          const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
+          cp_async16(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4), src);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
+      if (idx >= total || (!E4M3 && src_row[k] >= 0)) continue;
+      const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if constexpr (E4M3) {
+        if (src_row[k] >= 0) w = bf16x8_to_f16x8(v[k]);
+      }
+      *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = w;
+    }
+    cp_async_wait_all();
+    tc::fence_proxy_async_smem();
+  }
+  if (warp <= 8) asm volatile("bar.sync 1, 288;" ::: "memory");  // Q in shared memory
 
   if (E4M3 && warp == 9) {
     // ------------------------------------------------- producer (e4m3)
@@ -571,10 +601,11 @@ cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, E4M3, CAP>>(C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_pre, g.hkv);
-  prefill_kernel<D, E4M3, CAP><<<grid, C::kThreads, C::kSmem, st>>>(
-      g, p, layer, static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
-      static_cast<const uint8_t*>(vpool), kscale, vscale, static_cast<__nv_bfloat16*>(out), lse, acc, ml, err);
-  return cudaGetLastError();
+  e = launch_pdl(prefill_kernel<D, E4M3, CAP>, grid, C::kThreads, C::kSmem, st, g, p, layer,
+                 static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
+                 static_cast<const uint8_t*>(vpool), kscale, vscale, static_cast<__nv_bfloat16*>(out), lse, acc, ml,
+                 err);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -275,6 +275,42 @@ def fork_spec(name="fork_spec", seed=3, prompt=4096, n_forks=10, suffix_hi=256, 
     return w
 
 
+def nested_fork(name="nested_fork", seed=60, prompt=300, n_forks=4, sub_suffix=70, n_sub=4, suffix_hi=40,
+                drafts=4, num_layers=1, hq=32, hkv=8, d=128, kv_dtype=KV_BF16) -> Workload:
+    """A fork of a fork: a frozen prompt forked into n_forks working sets;
+    the first fork freezes a suffix of sub_suffix tokens and is forked again
+    into n_sub working sets.  Every leaf (the other forks and the sub-forks)
+    then freezes its own suffix of 1..suffix_hi tokens and attends a pass of
+    `drafts` speculative tokens.  The prompt is shared by every leaf; the
+    first fork's suffix by the sub-forks only."""
+    r = rng_for(seed, 0)
+    leaves = [f"a{i}" for i in range(1, n_forks)] + [f"b{i}" for i in range(n_sub)]
+    suffix = dict(zip(leaves, r.integers(1, suffix_hi + 1, len(leaves)).tolist()))
+    ops = []
+    w = Workload(name, seed, num_layers, hq, hkv, d, kv_dtype, 0, ops)
+    w.kv_streams["prompt"] = prompt
+    w.kv_streams["a0suf"] = sub_suffix
+    ops.append(("create", "root"))
+    ops.append(("pass", [("root", prompt, [("prompt", 0, prompt)], None, None)], False))
+    ops.append(("freeze", "root", -1))
+    ops += [("fork", "root", f"a{i}") for i in range(n_forks)]
+    ops.append(("pass", [("a0", sub_suffix, [("a0suf", 0, sub_suffix)], None, None)], False))
+    ops.append(("freeze", "a0", -1))
+    ops += [("fork", "a0", f"b{i}") for i in range(n_sub)]
+    for n in leaves:
+        w.kv_streams[f"suf_{n}"] = suffix[n]
+        w.kv_streams[f"draft_{n}"] = drafts
+        w.q_streams[f"dq_{n}"] = drafts
+    ops.append(("pass", [(n, suffix[n], [(f"suf_{n}", 0, suffix[n])], None, None) for n in leaves], False))
+    ops += [("freeze", n, -1) for n in leaves]
+    ops.append(("pass", [(n, drafts, [(f"draft_{n}", 0, drafts)], [(f"dq_{n}", 0, drafts)], None) for n in leaves],
+                True))
+    w.num_pages = (_pages_for([prompt]) + _pages_for([prompt + sub_suffix])
+                   + _pages_for([prompt + sub_suffix + suffix[n] + drafts for n in leaves]) + 32)
+    w.suffix = suffix
+    return w
+
+
 def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=2048,
                 ctx_lo=0, ctx_hi=4096, n_decode=128, dec_lo=1, dec_hi=4096,
                 num_layers=1, hq=32, hkv=8, d=128, kv_dtype=KV_BF16) -> Workload:
@@ -373,7 +409,7 @@ EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_bat
          "edge_batch", "edge_batch_e4m3",
          "mixed_batch_g16", "mixed_batch_e4m3_g16", "mixed_batch_mqa_g32", "mixed_batch_mqa_g64",
          "mixed_batch_e4m3_mqa_g64", "mixed_batch_d64_mqa_g16", "fork_spec_g16", "fork_spec_mqa_g32",
-         "llama70b_fp8_g16", "llama70b_fp8_mqa_g32")
+         "llama70b_fp8_g16", "llama70b_fp8_mqa_g32", "nested_fork", "nested_fork_e4m3")
 SOFTCAP_TEST = 3.0
 ROPE_THETA = 500000.0
 
@@ -456,6 +492,12 @@ def reduced(name: str) -> Workload:
         return decode_batch(name="llama70b_fp8_mqa_g32_small", seed=53, n_ws=8, ctx_lo=300, ctx_hi=1200,
                             num_layers=1, hq=32, hkv=1, d=128, kv_dtype=KV_E4M3, prefix_groups=4,
                             prefix_len=160)
+    if name in ("nested_fork", "nested_fork_e4m3"):
+        # the prompt's run: 7 leaves x 4 drafts x 4 heads on the tensor-core
+        # kernel; the first fork's suffix: 4 sub-forks x 4 x 4 = 64 on the
+        # decode kernel
+        return nested_fork(name=name + "_small", seed=60 + (name == "nested_fork_e4m3"),
+                           kv_dtype=KV_E4M3 if name.endswith("e4m3") else KV_BF16)
     if name == "edge_batch":
         return edge_batch()
     if name == "edge_batch_e4m3":

@@ -260,14 +260,60 @@ def test_plan_fork_group_reads_shared_pages_once():
     pre = pie.pie_batch_items(b, 1)
     dec = pie.pie_batch_items(b, 0)
     # 40 rows x 4 query heads per KV head = 160 > 64: shared prefix on the tensor-core kernel,
-    # one row tile (<= 256), KV split across items; every shared page in exactly one item
-    shared = [it for it in pre if it["key_base"] < 4096 and it["n_rows"] == 40]
-    assert shared and sum(it["n_pages"] for it in shared) == 4096 // 16
-    starts = sorted(it["key_base"] for it in shared)
-    assert starts[0] == 0
+    # in two balanced row tiles of 20 rows (one 128-row Q tile each), KV split across items;
+    # every shared page in exactly one item per row tile
+    shared = [it for it in pre if it["key_base"] < 4096 and it["n_rows"] == 20]
+    tiles = sorted({it["rows_off"] for it in shared})
+    assert len(tiles) == 2
+    for t in tiles:
+        mine = sorted((it["key_base"], it["n_pages"]) for it in shared if it["rows_off"] == t)
+        assert mine[0][0] == 0 and sum(n for _, n in mine) == 4096 // 16
+        for (a, n), (b2, _) in zip(mine, mine[1:]):
+            assert a + 16 * n == b2
     # private parts: one decode item (4 drafts x 4 heads = 16) per fork
     assert len([it for it in dec if it["n_rows"] == 4]) >= 10
     assert info["merge_rows"] == 40
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
+def test_plan_nested_forks_read_each_shared_run_once():
+    """A fork of a fork: the prompt's pages are in shared items over all 7
+    leaves' 28 rows, the first fork's own frozen pages in shared items over
+    its 4 sub-forks' 16 rows only, each page of each run in exactly one item
+    per row tile; every leaf's remaining pages are private."""
+    w = wl.reduced("nested_fork")
+    c, hs, b = _run_plan(w, 3)              # the drafts pass
+    pre, dec = pie.pie_batch_items(b, 1), pie.pie_batch_items(b, 0)
+    prompt_pages = 300 // 16                 # full pages of the prompt (18)
+    sub_pages = (300 + 70) // 16 - prompt_pages   # the first fork's full pages past the prompt (5)
+    top = [it for it in pre if it["n_rows"] == 28]
+    assert sorted((it["key_base"], it["n_pages"]) for it in top)[0][0] == 0
+    assert sum(it["n_pages"] for it in top) == prompt_pages
+    sub = [it for it in dec if it["n_rows"] == 16]
+    assert sum(it["n_pages"] for it in sub) == sub_pages
+    assert min(it["key_base"] for it in sub) == 16 * prompt_pages
+    # every leaf row has the prompt's parts, the sub-forks' rows also the sub-run's
+    info = pie.pie_batch_plan_info(b)
+    assert info["merge_rows"] == 28
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
+def test_plan_drafts_of_large_head_groups_still_share():
+    """Four drafts at 32 query heads per KV head (128 rows x heads) join the
+    fork group: the prompt is read once per pass, not once per fork."""
+    w = wl.reduced("fork_spec_mqa_g32")
+    c, hs, b = _run_plan(w, 2)
+    pre = pie.pie_batch_items(b, 1)
+    prompt_pages = 400 // 16
+    shared = [it for it in pre if it["key_base"] < 16 * prompt_pages]
+    tiles = sorted({it["rows_off"] for it in shared})
+    # 40 rows x 32 heads = 1280: ten row tiles of 4 rows (one Q tile each), each over the whole prompt
+    assert len(tiles) == 10 and all(it["n_rows"] == 4 for it in shared)
+    for t in tiles:
+        assert sum(it["n_pages"] for it in shared if it["rows_off"] == t) == prompt_pages
+    assert pie.pie_batch_plan_info(b)["merge_rows"] == 40
     pie.pie_batch_end(c, b)
     pie.pie_ctx_destroy(c)
 
