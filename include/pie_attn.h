@@ -266,7 +266,7 @@ pie_status pie_batch_end(pie_ctx* ctx, pie_batch* b);
  * device array of PIE_NOALLOC_SCRATCH_BYTES, which every GPU that loads the
  * library holds until the process exits.
  *  - Scratch needed, with R = num_rows and S = the KV splits the call picks
- *    (S >= 1): R*S*32 + 5*R*4 + (S > 1 ? R*S*Hq*(head_dim+2)*4 : 0) bytes
+ *    (S >= 1): R*S*32 + 7*R*4 + (S > 1 ? R*S*Hq*(head_dim+2)*4 : 0) bytes
  *    plus alignment; the call lowers S to fit and returns PIE_ERR_RANGE,
  *    with nothing launched, when even S = 1 does not fit.
  *  - The splits are sized from max_pages_per_row, so keep it tight (the

@@ -44,6 +44,12 @@ struct DecodeCfg {
   static constexpr int kEsize = E4M3 ? 1 : 2;
   static constexpr int kBlock = kPageSize * D * kEsize;  // bytes per page-head block
   static constexpr int kStages = E4M3 ? 12 : 8;
+  // Warps that take alternate pages (up to kConsumerWarps groups) must each
+  // own their stages: with the stage count a multiple of the group count a
+  // stage is only ever consumed by one warp, in order, so no warp can wait
+  // on a stage's phase before the previous phase of that stage completed
+  // (a parity wait cannot tell the two apart).
+  static_assert(kStages % kConsumerWarps == 0, "ring stages per page group");
   static constexpr int kStageBytes = 2 * kBlock;
   static constexpr int kNTW = NTW;   // N tiles (8 rows x heads each) per warp at most
   static constexpr int kMT = D / 16; // M tiles of the head dim in O^T
@@ -58,7 +64,7 @@ struct DecodeCfg {
 };
 
 template <bool E4M3, int D, bool CAP, int NTW>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(Geometry g, PlanView p, int layer,
+__global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geometry g, PlanView p, int layer,
                                                           const __nv_bfloat16* __restrict__ q,
                                                           const uint8_t* __restrict__ kpool,
                                                           const uint8_t* __restrict__ vpool,
@@ -478,7 +484,8 @@ __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__
   int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.n_merge * g.hq) return;
   int i = wid / g.hq, qh = wid % g.hq;
-  int row = p.merge_rows[i], np = p.merge_nparts[i], base = p.row_part_base[row];
+  const int4 mi = p.merge_info[i];  // one load: (row, parts, first part)
+  const int row = mi.x, np = mi.y, base = mi.z;
   auto ml_at = [&](int k) {
     return k < np ? *reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(base + k) * g.hq + qh) * 2)
                   : make_float2(-INFINITY, 0.f);
@@ -542,13 +549,14 @@ cudaError_t launch_decode_t(const Geometry& g, const PlanView& p, int layer, con
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Items of up to 32 rows x heads take one N tile per warp (fewer registers);
-// a launch with larger items (fork / dedup groups of 33-64) takes two.
+// Items of up to kDecodeNarrowM rows x heads take one N tile per warp (96
+// registers: 4 CTAs per SM where the shared memory allows, e4m3 pages); a
+// launch with wider items (fork / dedup groups of up to 64) takes two.
 template <bool E4M3, int D, bool CAP>
 cudaError_t launch_decode_n(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
                             const void* vpool, const float* ks, const float* vs, void* out, float* lse,
                             float* acc, float* ml, int* err, cudaStream_t st) {
-  return p.max_dec_m > 32
+  return p.max_dec_m > kDecodeNarrowM
              ? launch_decode_t<E4M3, D, CAP, 2>(g, p, layer, q, kpool, vpool, ks, vs, out, lse, acc, ml, err, st)
              : launch_decode_t<E4M3, D, CAP, 1>(g, p, layer, q, kpool, vpool, ks, vs, out, lse, acc, ml, err, st);
 }
@@ -619,7 +627,7 @@ void* g_noalloc_addr[kMaxDevices] = {};
 // the row's entries.
 __global__ void noalloc_plan(int n_rows, int n_splits, int chunk, int max_pages, const int32_t* __restrict__ seq_lens,
                              WorkItem* items, int32_t* row_pos, int32_t* row_list, int32_t* part_base,
-                             int32_t* merge_rows, int32_t* merge_np) {
+                             int4* merge_info) {
   pdl_wait();
   pdl_trigger();
   int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -643,15 +651,14 @@ __global__ void noalloc_plan(int n_rows, int n_splits, int chunk, int max_pages,
     row_pos[r] = len - 1;
     row_list[r] = r;
     part_base[r] = n_splits > 1 ? r * n_splits : -1;
-    merge_rows[r] = r;
-    merge_np[r] = n_splits;
+    merge_info[r] = make_int4(r, n_splits, r * n_splits, 0);
   }
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct NoAllocLayout {
-  size_t items, row_pos, row_list, part_base, merge_rows, merge_np, acc, ml, total;
+  size_t items, row_pos, row_list, part_base, merge_info, acc, ml, total;
 };
 
 NoAllocLayout noalloc_layout(int64_t R, int64_t S, int64_t hq, int64_t d) {
@@ -665,10 +672,8 @@ NoAllocLayout noalloc_layout(int64_t R, int64_t S, int64_t hq, int64_t d) {
   o = align256(o + R * 4);
   l.part_base = o;
   o = align256(o + R * 4);
-  l.merge_rows = o;
-  o = align256(o + R * 4);
-  l.merge_np = o;
-  o = align256(o + R * 4);
+  l.merge_info = o;
+  o = align256(o + R * 16);
   l.acc = o;
   if (S > 1) o = align256(o + R * S * hq * d * 4);
   l.ml = o;
@@ -725,14 +730,13 @@ extern "C" pie_status pie_attend_decode_noalloc(const pie_decode_args* a) {
   int32_t* row_pos = reinterpret_cast<int32_t*>(sc + lay.row_pos);
   int32_t* row_list = reinterpret_cast<int32_t*>(sc + lay.row_list);
   int32_t* part_base = reinterpret_cast<int32_t*>(sc + lay.part_base);
-  int32_t* merge_rows = reinterpret_cast<int32_t*>(sc + lay.merge_rows);
-  int32_t* merge_np = reinterpret_cast<int32_t*>(sc + lay.merge_np);
+  int4* merge_info = reinterpret_cast<int4*>(sc + lay.merge_info);
   float* acc = reinterpret_cast<float*>(sc + lay.acc);
   float* ml = reinterpret_cast<float*>(sc + lay.ml);
 
   const int n_items = R * S;
   if (launch_pdl(noalloc_plan, (n_items + 255) / 256, 256, 0, st, R, S, chunk, maxp, a->seq_lens, items, row_pos,
-                 row_list, part_base, merge_rows, merge_np) != cudaSuccess ||
+                 row_list, part_base, merge_info) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return PIE_ERR_CUDA;
 
@@ -745,8 +749,7 @@ extern "C" pie_status pie_attend_decode_noalloc(const pie_decode_args* a) {
   v.row_list = row_list;
   v.dec_items = items;
   v.pre_items = nullptr;
-  v.merge_rows = merge_rows;
-  v.merge_nparts = merge_np;
+  v.merge_info = merge_info;
   v.copies = nullptr;
   v.n_rows = R;
   v.n_dec = n_items;

@@ -180,7 +180,7 @@ pie_status ensure_device(pie_ctx* c, T** buf, size_t* cap, size_t need) {
 // -------------------------------------------------------------- planner
 struct PlanBuilder {
   std::vector<int32_t> page_ids, row_pos, row_slot, row_part_base, row_list;
-  std::vector<int32_t> merge_rows, merge_nparts;
+  std::vector<int4> merge_info;
   std::vector<CopyItem> copies;
   std::vector<WorkItem> dec, pre;
 };
@@ -409,8 +409,7 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
     if (n_parts[r] >= 2) {
       pb.row_part_base[r] = total;
       total += n_parts[r];
-      pb.merge_rows.push_back(r);
-      pb.merge_nparts.push_back(n_parts[r]);
+      pb.merge_info.push_back(make_int4(r, n_parts[r], pb.row_part_base[r], 0));
     }
   }
   for (auto& p : items) {
@@ -424,7 +423,11 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
     if (ca != cb) return ca > cb;
     return a.pages_off < b.pages_off;
   };
-  std::stable_sort(pb.dec.begin(), pb.dec.end(), [](const WorkItem& a, const WorkItem& b) {
+  // wide items (more than kDecodeNarrowM rows x heads) first, each kind
+  // longest first: the two kinds go to two launches of the decode kernel
+  std::stable_sort(pb.dec.begin(), pb.dec.end(), [G](const WorkItem& a, const WorkItem& b) {
+    const bool wa = a.n_rows * G > pie::kDecodeNarrowM, wb = b.n_rows * G > pie::kDecodeNarrowM;
+    if (wa != wb) return wa;
     return a.n_pages > b.n_pages;
   });
   std::stable_sort(pb.pre.begin(), pb.pre.end(), longer);
@@ -803,19 +806,24 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
   std::vector<uint8_t> blob;
   size_t o_pages = put(blob, pb.page_ids), o_pos = put(blob, pb.row_pos), o_slot = put(blob, pb.row_slot);
   size_t o_base = put(blob, pb.row_part_base), o_list = put(blob, pb.row_list);
-  size_t o_mr = put(blob, pb.merge_rows), o_mn = put(blob, pb.merge_nparts);
+  size_t o_mi = put(blob, pb.merge_info);
   size_t o_cp = put(blob, pb.copies), o_dec = put(blob, pb.dec, 32), o_pre = put(blob, pb.pre, 32);
   int64_t total_parts = 0;
-  for (int32_t n : pb.merge_nparts) total_parts += n;
+  for (const int4& mi : pb.merge_info) total_parts += mi.y;
 
   pie::PlanView& v = b->view;
   v.n_rows = b->n_rows;
   v.n_dec = static_cast<int32_t>(pb.dec.size());
   v.n_pre = static_cast<int32_t>(pb.pre.size());
-  v.n_merge = static_cast<int32_t>(pb.merge_rows.size());
+  v.n_merge = static_cast<int32_t>(pb.merge_info.size());
   v.n_copies = static_cast<int32_t>(pb.copies.size());
   v.max_dec_m = 0;
-  for (const WorkItem& it : pb.dec) v.max_dec_m = std::max(v.max_dec_m, it.n_rows * (c->geo.hq / c->geo.hkv));
+  v.n_dec_wide = 0;
+  for (const WorkItem& it : pb.dec) {
+    const int32_t m = it.n_rows * (c->geo.hq / c->geo.hkv);
+    v.max_dec_m = std::max(v.max_dec_m, m);
+    v.n_dec_wide += m > pie::kDecodeNarrowM;
+  }
   if (c->fail_next_begin) {
     c->fail_next_begin = false;
     undo_reservation(c, undo);
@@ -858,8 +866,7 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     v.row_slot = reinterpret_cast<const int32_t*>(d + o_slot);
     v.row_part_base = reinterpret_cast<const int32_t*>(d + o_base);
     v.row_list = reinterpret_cast<const int32_t*>(d + o_list);
-    v.merge_rows = reinterpret_cast<const int32_t*>(d + o_mr);
-    v.merge_nparts = reinterpret_cast<const int32_t*>(d + o_mn);
+    v.merge_info = reinterpret_cast<const int4*>(d + o_mi);
     v.copies = reinterpret_cast<const CopyItem*>(d + o_cp);
     v.dec_items = reinterpret_cast<const WorkItem*>(d + o_dec);
     v.pre_items = reinterpret_cast<const WorkItem*>(d + o_pre);
@@ -953,25 +960,41 @@ pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, vo
   size_t total_parts = c->part_cap / (static_cast<size_t>(c->geo.hq) * (c->geo.d + 2));
   float* ml = c->d_part + total_parts * c->geo.hq * c->geo.d;
   cudaError_t e = cudaSuccess;
-  // With both kinds of items, the decode launch goes on the side stream so
-  // it can take the SMs the tensor-core launch leaves free (a small pass
-  // fills only part of the GPU); the two write disjoint outputs and
-  // partials, and the merge waits for both.  The tensor-core grid is
+  // Up to three launches write disjoint outputs and partials: tensor-core
+  // items, wide decode items (fork / dedup groups of more than 32 rows x
+  // heads, two N tiles per warp) and narrow decode items.  The largest kind
+  // goes on the caller's stream -- tensor-core items if any, else the narrow
+  // decode items -- and the others on the context's second stream, forked
+  // from and joined back into the caller's stream, so they take the SMs the
+  // first leaves free; the merge waits for all.  The tensor-core grid is
   // submitted first: its CTAs need a whole SM each (224 KB of shared
   // memory), and decode CTAs spread over the SMs first would keep them out.
-  const bool both = v.n_pre && v.n_dec;
-  if (both) {
+  pie::PlanView wide = v, narrow = v;
+  wide.n_dec = v.n_dec_wide;
+  narrow.dec_items = v.dec_items + v.n_dec_wide;
+  narrow.n_dec = v.n_dec - v.n_dec_wide;
+  narrow.max_dec_m = std::min(v.max_dec_m, pie::kDecodeNarrowM);
+  const bool narrow_main = v.n_pre == 0;
+  const bool side = (v.n_pre > 0) + (wide.n_dec > 0) + (narrow.n_dec > 0) > 1;
+  if (side) {
     e = cudaEventRecord(c->fork_ev, c->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->side, c->fork_ev, 0);
   }
+  cudaStream_t other = side ? c->side : c->stream;
   if (e == cudaSuccess && v.n_pre)
     e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
                             lse, acc, ml, c->d_err, c->stream);
-  if (e == cudaSuccess && v.n_dec)
-    e = pie::launch_decode(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
-                           lse, acc, ml, c->d_err, both ? c->side : c->stream);
-  if (e == cudaSuccess && both) e = cudaEventRecord(c->join_ev, c->side);
-  if (e == cudaSuccess && both) e = cudaStreamWaitEvent(c->stream, c->join_ev, 0);
+  if (e == cudaSuccess && narrow.n_dec && narrow_main)
+    e = pie::launch_decode(c->geo, narrow, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc,
+                           out, lse, acc, ml, c->d_err, c->stream);
+  if (e == cudaSuccess && wide.n_dec)
+    e = pie::launch_decode(c->geo, wide, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
+                           lse, acc, ml, c->d_err, other);
+  if (e == cudaSuccess && narrow.n_dec && !narrow_main)
+    e = pie::launch_decode(c->geo, narrow, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc,
+                           out, lse, acc, ml, c->d_err, other);
+  if (e == cudaSuccess && side) e = cudaEventRecord(c->join_ev, c->side);
+  if (e == cudaSuccess && side) e = cudaStreamWaitEvent(c->stream, c->join_ev, 0);
   if (e == cudaSuccess && v.n_merge) e = pie::launch_merge(c->geo, v, out, lse, acc, ml, c->stream);
   if (e != cudaSuccess) return cuda_fail(c, e, "attend launch");
   return PIE_OK;

@@ -38,12 +38,19 @@ struct PlanView {
   const int32_t* row_list;       // item row lists
   const WorkItem* dec_items;     // decode-kernel items
   const WorkItem* pre_items;     // tensor-core (prefill) items
-  const int32_t* merge_rows;     // rows with >= 2 parts
-  const int32_t* merge_nparts;
+  const int4* merge_info;        // rows with >= 2 parts: (row, parts, first
+                                 // part index = row_part_base[row], 0)
   const CopyItem* copies;
   int32_t n_rows, n_dec, n_pre, n_merge, n_copies;
   int32_t max_dec_m;             // largest rows x query heads of a decode item
+  int32_t n_dec_wide;            // decode items [0, n_dec_wide) have more than
+                                 // kDecodeNarrowM rows x heads, the rest at most
 };
+
+// Decode items of at most this many rows x query heads run in the decode
+// kernel variant with one 8-wide N tile per warp (fewer registers, 4 CTAs
+// per SM); wider items (fork / dedup groups up to 64) take two per warp.
+constexpr int kDecodeNarrowM = 32;
 
 struct Geometry {
   int32_t num_layers, hq, hkv, d, num_pages, kv_dtype;
