@@ -478,7 +478,8 @@ __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__
   // One warp per (merged row, query head).  Lane k holds part k's (m, l)
   // (32 parts at a time), so the parts' loads are issued together; the
   // weights reach every lane by shuffle, and each lane accumulates E dims of
-  // the parts' partial outputs with vector loads, four parts in flight.
+  // the parts' partial outputs with vector loads (the first eight issued
+  // with the (m, l) loads, the rest four at a time).
   pdl_wait();
   pdl_trigger();
   int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -490,35 +491,59 @@ __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__
     return k < np ? *reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(base + k) * g.hq + qh) * 2)
                   : make_float2(-INFINITY, 0.f);
   };
+  constexpr int E = D / 32;
+  using Vec = typename std::conditional<E == 4, float4, float2>::type;
+  const float* a = part_acc + (static_cast<int64_t>(base) * g.hq + qh) * D + lane * E;
+  const int64_t part_stride = static_cast<int64_t>(g.hq) * D;
+  // The first kPre parts' partial outputs are loaded together with the (m, l)
+  // values (they do not depend on the weights): one round trip to L2 fewer
+  // before the sums, which is most of this kernel's time in a small pass.
+  constexpr int kPre = 8;
+  Vec pre[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    if (k < np) {
+      pre[k] = *reinterpret_cast<const Vec*>(a + k * part_stride);
+    } else {
+      reinterpret_cast<float*>(&pre[k])[0] = 0.f;
+      reinterpret_cast<float*>(&pre[k])[1] = 0.f;
+      if constexpr (E == 4) {
+        reinterpret_cast<float*>(&pre[k])[2] = 0.f;
+        reinterpret_cast<float*>(&pre[k])[3] = 0.f;
+      }
+    }
+  }
   const float2 ml0 = ml_at(lane);
   float m = ml0.x;
   for (int k0 = 32; k0 < np; k0 += 32) m = fmaxf(m, ml_at(k0 + lane).x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float base_m = m == -INFINITY ? 0.f : m;
-  constexpr int E = D / 32;
-  using Vec = typename std::conditional<E == 4, float4, float2>::type;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  auto add = [&](const Vec& v, float wk) {
+    acc[0] += v.x * wk;
+    acc[1] += v.y * wk;
+    if constexpr (E == 4) {
+      acc[2] += reinterpret_cast<const float4&>(v).z * wk;
+      acc[3] += reinterpret_cast<const float4&>(v).w * wk;
+    }
+  };
   float l = 0.f;
   for (int k0 = 0; k0 < np; k0 += 32) {
     const float2 ml = k0 == 0 ? ml0 : ml_at(k0 + lane);
     const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - base_m);
     l += ml.y * w;
     const int n = min(32, np - k0);
-    const float* a = part_acc + (static_cast<int64_t>(base + k0) * g.hq + qh) * D + lane * E;
-#pragma unroll 4
-    for (int kk = 0; kk < n; ++kk) {
-      const float wk = __shfl_sync(0xffffffffu, w, kk);
-      const Vec v = *reinterpret_cast<const Vec*>(a + static_cast<int64_t>(kk) * g.hq * D);
-      acc[0] += v.x * wk;
-      acc[1] += v.y * wk;
-      if constexpr (E == 4) {
-        acc[2] += reinterpret_cast<const float4&>(v).z * wk;
-        acc[3] += reinterpret_cast<const float4&>(v).w * wk;
-      }
+    if (k0 == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kPre; ++kk) add(pre[kk], __shfl_sync(0xffffffffu, w, kk));
     }
+    const int first = k0 == 0 ? kPre : 0;
+#pragma unroll 4
+    for (int kk = first; kk < n; ++kk)
+      add(*reinterpret_cast<const Vec*>(a + (k0 + kk) * part_stride), __shfl_sync(0xffffffffu, w, kk));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);

@@ -330,6 +330,25 @@ def test_plan_dedup_groups_on_decode_kernel():
     pie.pie_ctx_destroy(c)
 
 
+def test_plan_puts_wide_decode_items_first():
+    """Decode items of more than 32 rows x query heads (the dedup groups'
+    64-wide shared items) come first, each kind longest first: pie_attend
+    launches the two kinds separately (two N tiles per warp for the wide
+    ones) and relies on this order."""
+    w = wl.llama70b_fp8(n_ws=16, ctx_lo=2048, ctx_hi=4096, prefix_groups=2)
+    c, hs, b = _run_plan(w, 2)
+    G = w.num_q_heads // w.num_kv_heads
+    dec = pie.pie_batch_items(b, 0)
+    wide = [it["n_rows"] * G > 32 for it in dec]
+    n_wide = sum(wide)
+    assert n_wide > 0 and all(wide[:n_wide]) and not any(wide[n_wide:])
+    for part in (dec[:n_wide], dec[n_wide:]):
+        pages = [it["n_pages"] for it in part]
+        assert pages == sorted(pages, reverse=True)
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
+
+
 def test_plan_splits_cover_every_key_once():
     w = wl.decode_batch(name="split_plan", seed=7, n_ws=64, num_layers=1)
     c, hs, b = _run_plan(w, 1)
