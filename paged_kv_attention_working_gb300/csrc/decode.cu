@@ -162,10 +162,10 @@ __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geom
       uint32_t b0 = 0, b1 = 0;
       if (qp) {
         if constexpr (!E4M3) {
-          b0 = *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * tq);
-          b1 = *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * tq);
+          b0 = __ldcg(reinterpret_cast<const unsigned int*>(qp + 16 * ks + 2 * tq));
+          b1 = __ldcg(reinterpret_cast<const unsigned int*>(qp + 16 * ks + 8 + 2 * tq));
         } else {
-          const uint2 w = *reinterpret_cast<const uint2*>(qp + 16 * ks + 4 * tq);
+          const uint2 w = __ldcg(reinterpret_cast<const uint2*>(qp + 16 * ks + 4 * tq));
           b0 = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
           b1 = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
         }
