@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geom
     const int mq = 8 * (C::kNTW * ow + i) + gq;
     const __nv_bfloat16* qp = nullptr;
     if (i < ntw && mq < M)
-      qp = q + (static_cast<int64_t>(p.row_list[it.rows_off + mq / G]) * g.hq + head * G + mq % G) * D;
+      qp = q + (static_cast<int64_t>(item_row(p, it, mq / G)) * g.hq + head * G + mq % G) * D;
 #pragma unroll
     for (int ks = 0; ks < C::kKS; ++ks) {
       uint32_t b0 = 0, b1 = 0;
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geom
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int m = 8 * (C::kNTW * ow + i) + 2 * tq + e;
-      colpos[i][e] = i < ntw && m < M ? p.row_pos[p.row_list[it.rows_off + m / G]] : -1;
+      colpos[i][e] = i < ntw && m < M ? p.row_pos[item_row(p, it, m / G)] : -1;
     }
   }
 
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geom
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int m = 8 * nt + 2 * tq + e;
-      colrow[e] = m < M ? p.row_list[it.rows_off + m / G] : -1;
+      colrow[e] = m < M ? item_row(p, it, m / G) : -1;
       colqh[e] = head * G + m % G;
     }
     if (it.part < 0) {
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geom
         // 2t+1): each lane then stores whole bf16 pairs of one head
         const int m = 8 * nt + gq;
         __nv_bfloat16* dst =
-            m < M ? out + (static_cast<int64_t>(p.row_list[it.rows_off + m / G]) * g.hq + head * G + m % G) * D
+            m < M ? out + (static_cast<int64_t>(item_row(p, it, m / G)) * g.hq + head * G + m % G) * D
                   : nullptr;
 #pragma unroll
         for (int mt = 0; mt < C::kMT; ++mt) {
@@ -670,7 +670,7 @@ __global__ void noalloc_plan(int n_rows, int n_splits, int chunk, int max_pages,
   it.n_rows = 1;
   it.part = n_splits > 1 ? s : -1;
   it.n_keys = max(0, min(np * kPageSize, len - first * kPageSize));
-  it.pad = 0;
+  it.direct_rows = 1;  // row_list[r] = r
   items[i] = it;
   if (s == 0) {
     row_pos[r] = len - 1;

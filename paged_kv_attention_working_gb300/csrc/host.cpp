@@ -379,6 +379,7 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
         it.n_keys = std::min(sp[j].second * kPageSize, s.n0 + s.n_new - it.key_base);
         it.rows_off = s.row0;  // row_list[0..n_rows) is the identity
         it.n_rows = s.n_new;
+        it.direct_rows = 1;
         it.part = base_part + static_cast<int32_t>(j);
         items.push_back({it, true});
       }
@@ -395,6 +396,7 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
         it.n_keys = last_pos + 1 - it.key_base;
         it.rows_off = s.row0 + r0;
         it.n_rows = nr;
+        it.direct_rows = 1;
         it.part = base_part;
         items.push_back({it, false});
         for (int32_t r = 0; r < nr; ++r) n_parts[s.row0 + r0 + r] += 1;

@@ -21,7 +21,9 @@ struct WorkItem {
   int32_t part;       // -1: rows are written straight to the output;
                       // else partial index = row_part_base[row] + part
   int32_t n_keys;     // keys in the run that lie before its end (<= 16*n_pages)
-  int32_t pad;
+  int32_t direct_rows;  // 1: the item's rows are batch rows rows_off,
+                        // rows_off + 1, ... in order (row_list is the
+                        // identity there), so a kernel skips the lookup
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
@@ -46,6 +48,13 @@ struct PlanView {
   int32_t n_dec_wide;            // decode items [0, n_dec_wide) have more than
                                  // kDecodeNarrowM rows x heads, the rest at most
 };
+
+#ifdef __CUDACC__
+// Batch row of an item's i-th row.
+__device__ __forceinline__ int item_row(const PlanView& p, const WorkItem& it, int i) {
+  return it.direct_rows ? it.rows_off + i : p.row_list[it.rows_off + i];
+}
+#endif
 
 // Decode items of at most this many rows x query heads run in the decode
 // kernel variant with one 8-wide N tile per warp (fewer registers, 4 CTAs

@@ -83,6 +83,9 @@ struct PreCfg {
   static constexpr uint32_t kColO = 256;
 };
 
+// Position given to rows past an item's last row: after every key.
+constexpr int kNoRowPos = 0x3fffffff;
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -210,6 +213,38 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
+
+  // Q tiles -> shared memory, 128-byte swizzled K-major, rows past M zero;
+  // loaded by the softmax warps while the producers already fetch K and V.
+  // Every load of a thread is in flight at once (16-byte cp.async copies,
+  // or, for e4m3 contexts, register loads for the f16 conversion, issued
+  // before the barriers and tensor memory are set up); a load loop that
+  // waited for each copy in turn cost a few microseconds per CTA, the whole
+  // run time of a short item.  The MMA thread issues no product before the
+  // named barrier below.
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  constexpr int kPer = 2 * 128 * kChunks / 256;
+  const int q_total = n_qt * 128 * kChunks;
+  // e4m3: every row first, then every load (-1: past M, stays zero)
+  int e_row[E4M3 ? kPer : 1];
+  uint4 e_val[E4M3 ? kPer : 1];
+  if constexpr (E4M3) {
+    if (warp < 8) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + 256 * k, m = idx / kChunks;
+        e_row[k] = idx < q_total && m < M ? item_row(p, it, m / G) : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
+        if (e_row[k] >= 0)
+          e_val[k] = *reinterpret_cast<const uint4*>(
+              q + (static_cast<int64_t>(e_row[k]) * g.hq + head * G + m % G) * D + c16 * 8);
+      }
+    }
+  }
+
   if (warp == 8) {
     tc::alloc(tmem_slot, C::kTmemCols);
     tc::relinquish();
@@ -219,47 +254,39 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Q tiles -> shared memory, 128-byte swizzled K-major, rows past M zero;
-  // loaded by the softmax warps while the producers already fetch K and V.
-  // Every load of a thread is in flight at once (row indices first, then
-  // 16-byte cp.async copies, or register loads for the f16 conversion of
-  // e4m3 contexts); a load loop that waited for each copy in turn cost a
-  // few microseconds per CTA, the whole run time of a short item.  The MMA
-  // thread issues no product before the named barrier below.
   if (warp < 8) {
-    constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    constexpr int kPer = 2 * 128 * kChunks / 256;
-    const int total = n_qt * 128 * kChunks;
-    int src_row[kPer];
+    if constexpr (E4M3) {
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = threadIdx.x + 256 * k, m = idx / kChunks;
-      src_row[k] = idx < total && m < M ? p.row_list[it.rows_off + m / G] : -1;
-    }
-    uint4 v[E4M3 ? kPer : 1];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
-      if (src_row[k] >= 0) {
-        const __nv_bfloat16* src = q + (static_cast<int64_t>(src_row[k]) * g.hq + head * G + m % G) * D + c16 * 8;
-        if constexpr (E4M3) {
-          v[k] = *reinterpret_cast<const uint4*>(src);
-        } else {
-          const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
-          cp_async16(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4), src);
-        }
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
+        if (idx >= q_total) continue;
+        const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
+        const uint4 w = e_row[k] >= 0 ? bf16x8_to_f16x8(e_val[k]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = w;
       }
-    }
+    } else {
+      int src_row[kPer];
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
-      if (idx >= total || (!E4M3 && src_row[k] >= 0)) continue;
-      const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if constexpr (E4M3) {
-        if (src_row[k] >= 0) w = bf16x8_to_f16x8(v[k]);
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + 256 * k, m = idx / kChunks;
+        src_row[k] = idx < q_total && m < M ? item_row(p, it, m / G) : -1;
       }
-      *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = w;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
+        if (src_row[k] < 0) continue;
+        const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
+        cp_async16(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4),
+                   q + (static_cast<int64_t>(src_row[k]) * g.hq + head * G + m % G) * D + c16 * 8);
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + 256 * k, m = idx / kChunks, c16 = idx % kChunks;
+        if (idx >= q_total || src_row[k] >= 0) continue;
+        const int t = m >> 7, r = m & 127, panel = c16 >> 3, c = c16 & 7;
+        *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(0, 0, 0, 0);
+      }
     }
     cp_async_wait_all();
     tc::fence_proxy_async_smem();
@@ -458,12 +485,18 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     const int m = t * 128 + r;
     const uint32_t row_s = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16) + t * C::kKeys;
     const uint32_t row_o = tmem + (static_cast<uint32_t>((warp & 3) << 5) << 16) + C::kColO + t * D;
-    int row = -1, pos = -1, qh = 0;
+    // rows past M (zero Q) take a position past every key, so that they do
+    // not force the masked path on their warp; their results are dropped
+    int row = -1, pos = kNoRowPos, qh = 0;
     if (m < M) {
-      row = p.row_list[it.rows_off + m / G];
+      row = item_row(p, it, m / G);
       pos = p.row_pos[row];
       qh = head * G + m % G;
     }
+    // a warp with no row below M computes nothing: it only keeps the
+    // barrier protocol (the P lanes it leaves hold S values, which reach
+    // only the O rows of those lanes, never stored)
+    const bool idle = __all_sync(0xffffffffu, row < 0);
     // scores in log2 units: s * qk_scale; with the soft cap c the scores
     // are first mapped to tanh(s * cap_pre) and then scaled by
     // qk_scale = c * log2(e) (c * tanh(s / c) in log2 units)
@@ -475,6 +508,11 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     for (int j = 0; j < nkv && ok; ++j) {
       ok = warp_wait(&s_full[t], j & 1, err);
       if (!ok) break;
+      if (idle) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
+        continue;
+      }
       tc::fence_after();
       // columns <= lim are visible: causal, and inside the item's key run
       // (the tile past the run's end holds stand-in pages)
@@ -545,17 +583,36 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     }
     if (ok) ok = warp_wait(&o_done[t], (nkv - 1) & 1, err);
     tc::fence_after();
-    if (ok) {
+    if (ok && !idle) {
+      // O of the warp's 32 rows goes out through shared memory: each lane
+      // writes its row (tensor-memory lane) into the warp's quarter of Q
+      // tile t's buffer (free: every S_t has completed), in 16-byte chunks
+      // XOR-swizzled by row so that neither the row-wise writes nor the
+      // chunk-wise reads meet a bank conflict; then 32 / kCh lanes store one
+      // row per instruction, each 32-byte sector of the output written
+      // whole.  (Storing each lane's own row straight from registers wrote
+      // 32 half sectors per instruction and took about 4,000 cycles per CTA.)
+      // Direct rows stage the bf16 row (2d bytes) once, split rows their
+      // fp32 partial in two halves of 2d bytes.
+      constexpr int kRowB = 2 * D;     // staged bytes per row and round
+      constexpr int kCh = kRowB / 16;  // 16-byte chunks per staged row
+      constexpr int kRpi = 32 / kCh;   // rows per store instruction
+      static_assert(4 * 32 * kRowB == C::kQTile, "staging fills the Q tile buffer");
+      uint8_t* stage = smem + C::kOffQ + t * C::kQTile + (warp & 3) * 32 * kRowB;
+      auto put = [&](int c, uint4 w) {
+        *reinterpret_cast<uint4*>(stage + lane * kRowB + ((c ^ (lane % kCh)) << 4)) = w;
+      };
+      auto get = [&](int rr, int c) {
+        return *reinterpret_cast<const uint4*>(stage + rr * kRowB + ((c ^ (rr % kCh)) << 4));
+      };
       const float vdq = E4M3 ? vscale[layer * g.hkv + head] : 1.0f;
-      const float inv = l_run > 0.f ? vdq / l_run : 0.f;
+      if (it.part < 0) {
+        const float inv = l_run > 0.f ? vdq / l_run : 0.f;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tc::ld32(row_o + cc * 32, o);
-        tc::wait_ld();
-        if (row < 0) continue;
-        if (it.part < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(row) * g.hq + qh) * D + cc * 32);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tc::ld32(row_o + cc * 32, o);
+          tc::wait_ld();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
@@ -563,24 +620,46 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
             w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
             w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
             w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = w;
+            put(4 * cc + v, w);
           }
-        } else {
-          const int64_t slot = static_cast<int64_t>(p.row_part_base[row] + it.part) * g.hq + qh;
-          float4* dst = reinterpret_cast<float4*>(part_acc + slot * D + cc * 32);
+        }
+        __syncwarp();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * vdq, __uint_as_float(o[4 * v + 1]) * vdq,
-                                 __uint_as_float(o[4 * v + 2]) * vdq, __uint_as_float(o[4 * v + 3]) * vdq);
+        for (int i = 0; i < kCh; ++i) {
+          const int rr = i * kRpi + lane / kCh, c = lane % kCh;
+          const int rrow = __shfl_sync(0xffffffffu, row, rr), rqh = __shfl_sync(0xffffffffu, qh, rr);
+          const uint4 w = get(rr, c);
+          if (rrow >= 0) *reinterpret_cast<uint4*>(out + (static_cast<int64_t>(rrow) * g.hq + rqh) * D + c * 8) = w;
         }
-      }
-      if (row >= 0) {
-        if (it.part < 0) {
-          if (lse) lse[static_cast<int64_t>(row) * g.hq + qh] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
-        } else {
-          const int64_t slot = static_cast<int64_t>(p.row_part_base[row] + it.part) * g.hq + qh;
-          *reinterpret_cast<float2*>(part_ml + slot * 2) = make_float2(m_run, l_run);
+        if (row >= 0 && lse) lse[static_cast<int64_t>(row) * g.hq + qh] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+      } else {
+        const int slot = row >= 0 ? (p.row_part_base[row] + it.part) * g.hq + qh : -1;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t o[32];
+            tc::ld32(row_o + half * (D / 2) + cc * 32, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              put(8 * cc + v, make_uint4(__float_as_uint(__uint_as_float(o[4 * v]) * vdq),
+                                         __float_as_uint(__uint_as_float(o[4 * v + 1]) * vdq),
+                                         __float_as_uint(__uint_as_float(o[4 * v + 2]) * vdq),
+                                         __float_as_uint(__uint_as_float(o[4 * v + 3]) * vdq)));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < kCh; ++i) {
+            const int rr = i * kRpi + lane / kCh, c = lane % kCh;
+            const int rslot = __shfl_sync(0xffffffffu, slot, rr);
+            const uint4 w = get(rr, c);
+            if (rslot >= 0)
+              *reinterpret_cast<uint4*>(part_acc + static_cast<int64_t>(rslot) * D + half * (D / 2) + c * 4) = w;
+          }
+          __syncwarp();  // the next half overwrites the staging rows
         }
+        if (row >= 0) *reinterpret_cast<float2*>(part_ml + static_cast<int64_t>(slot) * 2) = make_float2(m_run, l_run);
       }
     }
   }
