@@ -314,7 +314,9 @@ pie_status pie_batch_plan_info(const pie_batch* b, int32_t* info);
 /* Copies work items (kind 0: decode kernel, 1: tensor-core kernel), 8 int32
  * each: first page index into the batch's page list, pages, first key
  * position, first row-list index, rows, part (-1 = direct output), keys,
- * reserved.  *n = total items; at most cap are copied. */
+ * and 1 when the item's rows are the consecutive batch rows starting at the
+ * row-list index (the list is the identity there), else 0.  *n = total
+ * items; at most cap are copied. */
 pie_status pie_batch_items(const pie_batch* b, int32_t kind, int32_t* out, int32_t cap,
                            int32_t* n);
 /* Synchronises the stream and returns (and clears) the kernels' error bits:

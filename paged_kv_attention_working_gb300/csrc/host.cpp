@@ -315,6 +315,17 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
     for (int32_t i : g.members)
       for (int32_t r = 0; r < segs[i].n_new; ++r) pb.row_list.push_back(segs[i].row0 + r);
     int32_t rows = static_cast<int32_t>(pb.row_list.size()) - rows_off;
+    // members whose rows are consecutive batch rows (a fork group's drafts,
+    // usually) are addressed through the identity prefix of row_list, so
+    // the kernels skip the lookup
+    bool consecutive = true;
+    for (int32_t r = 1; r < rows && consecutive; ++r)
+      consecutive = pb.row_list[rows_off + r] == pb.row_list[rows_off] + r;
+    if (consecutive) {
+      const int32_t first = pb.row_list[rows_off];
+      pb.row_list.resize(rows_off);
+      rows_off = first;
+    }
     const SegInfo& s0 = segs[g.members[0]];
     const int32_t run = g.p1 - g.p0;
     bool decode = static_cast<int64_t>(rows) * G <= kDecodeSharedMaxM;
@@ -353,6 +364,7 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
         it.n_keys = sp[j].second * kPageSize;
         it.rows_off = rows_off + r0;
         it.n_rows = nr;
+        it.direct_rows = consecutive ? 1 : 0;
         it.part = base_part + static_cast<int32_t>(j);
         items.push_back({it, decode});
       }

@@ -287,8 +287,8 @@ def pie_batch_items(batch, kind):
     _check(None, lib.pie_batch_items(batch, kind, None, 0, ctypes.byref(n)), "pie_batch_items")
     buf = (ctypes.c_int32 * max(1, 8 * n.value))()
     _check(None, lib.pie_batch_items(batch, kind, buf, n.value, ctypes.byref(n)), "pie_batch_items")
-    keys = ("pages_off", "n_pages", "key_base", "rows_off", "n_rows", "part", "n_keys")
-    return [dict(zip(keys, buf[8 * i: 8 * i + 7])) for i in range(n.value)]
+    keys = ("pages_off", "n_pages", "key_base", "rows_off", "n_rows", "part", "n_keys", "direct_rows")
+    return [dict(zip(keys, buf[8 * i: 8 * i + 8])) for i in range(n.value)]
 
 
 def pie_kv_append(ctx, batch, layer, k, v) -> None:

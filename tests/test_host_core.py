@@ -429,3 +429,36 @@ def test_plan_prefill_chunks_never_join_groups():
     assert info["merge_rows"] == 0 and info["prefill_items"] > 0
     pie.pie_batch_end(c, b)
     pie.pie_ctx_destroy(c)
+
+
+def test_plan_marks_consecutive_rows_direct():
+    """Items whose rows are consecutive batch rows carry the direct flag and
+    index the identity prefix of the row list: a segment's private items,
+    and a fork group whose members sit next to each other in the pass.  A
+    group split by another segment keeps its own row list."""
+    cfg = dict(num_layers=1, num_q_heads=8, num_kv_heads=2, head_dim=64, num_pages=64)
+    for order, consecutive in (("ffu", True), ("fuf", False)):
+        c = pie.pie_ctx_create(**cfg)
+        prompt = pie.pie_ws_create(c)
+        b = pie.pie_batch_begin(c, [(prompt, 64, None)])
+        pie.pie_batch_end(c, b)
+        pie.pie_ws_freeze(c, prompt)
+        f1, f2 = pie.pie_ws_fork(c, prompt), pie.pie_ws_fork(c, prompt)
+        u = pie.pie_ws_create(c)
+        ws = {"f": [f1, f2], "u": [u]}
+        segs = [(ws[k].pop(0), 3, None) for k in order]
+        b = pie.pie_batch_begin(c, segs)
+        items = pie.pie_batch_items(b, 0) + pie.pie_batch_items(b, 1)
+        shared = [it for it in items if it["n_rows"] == 6]
+        assert shared, "the fork group's prompt pages form a shared item"
+        for it in shared:
+            assert it["direct_rows"] == (1 if consecutive else 0)
+            if consecutive:
+                assert it["rows_off"] == 0        # rows 0..5, the identity prefix
+            else:
+                assert it["rows_off"] >= 9        # a list of its own after the 9 batch rows
+        for it in items:
+            if it["n_rows"] == 3:                  # private items: each segment's own rows
+                assert it["direct_rows"] == 1 and it["rows_off"] % 3 == 0
+        pie.pie_batch_end(c, b)
+        pie.pie_ctx_destroy(c)
