@@ -311,6 +311,46 @@ def nested_fork(name="nested_fork", seed=60, prompt=300, n_forks=4, sub_suffix=7
     return w
 
 
+def interleaved_forks(name="interleaved_forks", seed=70, prompt_a=300, prompt_b=200, n_forks=3, drafts_a=8,
+                      drafts_b=2, suffix_hi=40, num_layers=1, hq=32, hkv=8, d=128, kv_dtype=KV_BF16) -> Workload:
+    """Two frozen prompts, each forked into n_forks working sets that freeze
+    their own suffixes of 1..suffix_hi tokens; the drafts pass then lists the
+    forks alternately (a0, b0, a1, b1, ...), so neither fork group's rows are
+    consecutive batch rows.  Group a (n_forks x drafts_a rows) is sized for
+    the tensor-core kernel, group b (n_forks x drafts_b rows) for the decode
+    kernel's shared items."""
+    r = rng_for(seed, 0)
+    a = [f"a{i}" for i in range(n_forks)]
+    b = [f"b{i}" for i in range(n_forks)]
+    leaves = [x for pair in zip(a, b) for x in pair]
+    suffix = dict(zip(leaves, r.integers(1, suffix_hi + 1, len(leaves)).tolist()))
+    drafts = {n: (drafts_a if n in a else drafts_b) for n in leaves}
+    ops = []
+    w = Workload(name, seed, num_layers, hq, hkv, d, kv_dtype, 0, ops)
+    for root, n_tok in (("pa", prompt_a), ("pb", prompt_b)):
+        w.kv_streams[root] = n_tok
+        ops.append(("create", root))
+        ops.append(("pass", [(root, n_tok, [(root, 0, n_tok)], None, None)], False))
+        ops.append(("freeze", root, -1))
+    ops += [("fork", "pa", n) for n in a] + [("fork", "pb", n) for n in b]
+    for n in leaves:
+        w.kv_streams[f"suf_{n}"] = suffix[n]
+        w.q_streams[f"sq_{n}"] = suffix[n]
+        w.kv_streams[f"draft_{n}"] = drafts[n]
+        w.q_streams[f"dq_{n}"] = drafts[n]
+    # both passes attend: the suffixes' rows also read their prompt through
+    # the groups' own row lists
+    ops.append(("pass", [(n, suffix[n], [(f"suf_{n}", 0, suffix[n])], [(f"sq_{n}", 0, suffix[n])], None)
+                         for n in leaves], True))
+    ops += [("freeze", n, -1) for n in leaves]
+    ops.append(("pass", [(n, drafts[n], [(f"draft_{n}", 0, drafts[n])], [(f"dq_{n}", 0, drafts[n])], None)
+                         for n in leaves], True))
+    w.num_pages = (_pages_for([prompt_a, prompt_b])
+                   + _pages_for([(prompt_a if n in a else prompt_b) + suffix[n] + drafts[n] for n in leaves]) + 32)
+    w.suffix = suffix
+    return w
+
+
 def mixed_batch(name="mixed_batch", seed=4, n_chunks=16, chunk_lo=512, chunk_hi=2048,
                 ctx_lo=0, ctx_hi=4096, n_decode=128, dec_lo=1, dec_hi=4096,
                 num_layers=1, hq=32, hkv=8, d=128, kv_dtype=KV_BF16) -> Workload:
@@ -409,7 +449,8 @@ EXTRA = ("fork_spec_e4m3", "mixed_batch_e4m3", "mixed_batch_softcap", "mixed_bat
          "edge_batch", "edge_batch_e4m3",
          "mixed_batch_g16", "mixed_batch_e4m3_g16", "mixed_batch_mqa_g32", "mixed_batch_mqa_g64",
          "mixed_batch_e4m3_mqa_g64", "mixed_batch_d64_mqa_g16", "fork_spec_g16", "fork_spec_mqa_g32",
-         "llama70b_fp8_g16", "llama70b_fp8_mqa_g32", "nested_fork", "nested_fork_e4m3")
+         "llama70b_fp8_g16", "llama70b_fp8_mqa_g32", "nested_fork", "nested_fork_e4m3",
+         "interleaved_forks", "interleaved_forks_e4m3")
 SOFTCAP_TEST = 3.0
 ROPE_THETA = 500000.0
 
@@ -498,6 +539,12 @@ def reduced(name: str) -> Workload:
         # decode kernel
         return nested_fork(name=name + "_small", seed=60 + (name == "nested_fork_e4m3"),
                            kv_dtype=KV_E4M3 if name.endswith("e4m3") else KV_BF16)
+    if name in ("interleaved_forks", "interleaved_forks_e4m3"):
+        # two fork groups listed alternately: the first (3 forks x 8 drafts x 4
+        # heads = 96) on the tensor-core kernel, the second (3 x 2 x 4 = 24) on
+        # the decode kernel, both through their own row lists
+        e4 = name.endswith("e4m3")
+        return interleaved_forks(name=name + "_small", seed=70 + e4, kv_dtype=KV_E4M3 if e4 else KV_BF16)
     if name == "edge_batch":
         return edge_batch()
     if name == "edge_batch_e4m3":
