@@ -8,6 +8,8 @@
 // packing of many passes into shared launches ("How Pie thinks", "Batching
 // is still the engine's job") and the role of ops.attn.plan_prefill ("Poem
 // ops", Operations table).
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <array>
 #include <cmath>
@@ -106,6 +108,10 @@ struct pie_ctx {
   // items (fork: side waits on main; join: main waits on side)
   cudaStream_t side = nullptr;
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  // the last Q tensor map built, for the Q pointer and row count it covers
+  CUtensorMap q_map{};
+  const void* q_map_ptr = nullptr;
+  int32_t q_map_rows = -1;
   bool upload_pending = false;
   float* d_part = nullptr;  // partial (acc | m,l) results
   size_t part_cap = 0;      // floats
@@ -962,6 +968,48 @@ pie_status pie_kv_append_rope(pie_ctx* c, pie_batch* b, int32_t layer, const voi
   return PIE_OK;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null when the driver does not offer it.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult found{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &found) !=
+            cudaSuccess ||
+        found != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Tensor map over a bf16 Q ([n_rows][Hq][d]) for the tensor-core kernel's Q
+// tiles: box d 64 x G heads x 128/G rows with the 128-byte swizzle, which is
+// the tiles' K-major operand layout.  False when it cannot be built; the
+// kernel then loads Q by cp.async.
+static bool q_tensor_map(pie_ctx* c, const void* q, int32_t n_rows, CUtensorMap* map) {
+  if (q == c->q_map_ptr && n_rows == c->q_map_rows) {
+    *map = c->q_map;
+    return true;
+  }
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || c->geo.kv_dtype != PIE_KV_BF16 || (reinterpret_cast<uintptr_t>(q) & 15) != 0) return false;
+  const cuuint64_t d = static_cast<cuuint64_t>(c->geo.d), hq = static_cast<cuuint64_t>(c->geo.hq);
+  const cuuint32_t G = static_cast<cuuint32_t>(c->geo.hq / c->geo.hkv);
+  const cuuint64_t dim[3] = {d, hq, static_cast<cuuint64_t>(n_rows)};
+  const cuuint64_t stride[2] = {d * 2, hq * d * 2};  // bytes, dimensions 1 and 2
+  const cuuint32_t box[3] = {64, G, 128 / G};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dim, stride, box, elem,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  c->q_map = *map;
+  c->q_map_ptr = q;
+  c->q_map_rows = n_rows;
+  return true;
+}
+
 pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, void* out, float* lse) {
   if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
   if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
@@ -995,9 +1043,16 @@ pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, vo
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->side, c->fork_ev, 0);
   }
   cudaStream_t other = side ? c->side : c->stream;
-  if (e == cudaSuccess && v.n_pre)
-    e = pie::launch_prefill(c->geo, v, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc, out,
-                            lse, acc, ml, c->d_err, c->stream);
+  if (e == cudaSuccess && v.n_pre) {
+    // The map costs microseconds of host time per new Q address; it is built
+    // when the tensor-core launch runs more than one wave of CTAs (a
+    // one-wave launch is short, and the pass then waits on the host)
+    CUtensorMap q_map;
+    const bool mapped = static_cast<int64_t>(v.n_pre) * c->geo.hkv > c->num_sms &&
+                        q_tensor_map(c, q, b->n_rows, &q_map);
+    e = pie::launch_prefill(c->geo, v, layer, q, mapped ? &q_map : nullptr, c->cfg.k_pool, c->cfg.v_pool,
+                            c->d_scales, c->d_scales + nsc, out, lse, acc, ml, c->d_err, c->stream);
+  }
   if (e == cudaSuccess && narrow.n_dec && narrow_main)
     e = pie::launch_decode(c->geo, narrow, layer, q, c->cfg.k_pool, c->cfg.v_pool, c->d_scales, c->d_scales + nsc,
                            out, lse, acc, ml, c->d_err, c->stream);

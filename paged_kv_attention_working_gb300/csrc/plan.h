@@ -1,6 +1,7 @@
 // Internal plan structures shared by the host planner and the CUDA kernels.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace pie {
@@ -82,10 +83,13 @@ cudaError_t launch_decode(const Geometry& g, const PlanView& p, int layer, const
                           const void* kpool, const void* vpool, const float* scale_k,
                           const float* scale_v, void* out, float* lse, float* part_acc,
                           float* part_ml, int* err, cudaStream_t st);
+// q_map: a tiled tensor map over Q ([rows][Hq][d] bf16, box d 64 x G heads x
+// 128/G rows, 128-byte swizzle), or null; with it, items whose rows are in
+// batch order load their Q tiles by tensor copies.
 cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, const void* q,
-                           const void* kpool, const void* vpool, const float* scale_k,
-                           const float* scale_v, void* out, float* lse, float* part_acc,
-                           float* part_ml, int* err, cudaStream_t st);
+                           const CUtensorMap* q_map, const void* kpool, const void* vpool,
+                           const float* scale_k, const float* scale_v, void* out, float* lse,
+                           float* part_acc, float* part_ml, int* err, cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint32_t polls, cudaStream_t st);
 cudaError_t launch_merge(const Geometry& g, const PlanView& p, void* out, float* lse,
                          const float* part_acc, const float* part_ml, cudaStream_t st);

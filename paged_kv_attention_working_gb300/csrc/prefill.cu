@@ -77,7 +77,7 @@ struct PreCfg {
   static constexpr int kOffV = kOffK + kKStages * kKVTile;
   static constexpr int kOffRaw = kOffV + kVStages * kKVTile;
   static constexpr int kOffBar = kOffRaw + kRawStages * kRawTile;
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 * kRawStages + 1;
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 * kRawStages + 2;
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
@@ -159,6 +159,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
 template <int D, bool E4M3, bool CAP>
 __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     prefill_kernel(Geometry g, PlanView p, int layer, const __nv_bfloat16* __restrict__ q,
+                   const __grid_constant__ CUtensorMap q_map, int q_tma,
                    const uint8_t* __restrict__ kpool, const uint8_t* __restrict__ vpool,
                    const float* __restrict__ kscale, const float* __restrict__ vscale,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_acc,
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
   uint64_t* raw_full = o_done + 2;                // [raw stage] (e4m3 only)
   uint64_t* raw_empty = raw_full + C::kRawStages;
   uint64_t* mma_drain = raw_empty + C::kRawStages;  // every issued MMA complete
+  uint64_t* q_full = mma_drain + 1;                 // Q tiles landed (tensor-copy path)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const WorkItem it = p.pre_items[blockIdx.x];
@@ -190,6 +192,11 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
   const int n_qt = M > 128 ? 2 : 1;
   const int nkv = (it.n_keys + C::kKeys - 1) / C::kKeys;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // bf16 items whose rows are in batch order take their Q tiles by tensor
+  // copies (the MMA thread issues them); the others by the softmax warps'
+  // cp.async copies, which the SM keeps only so many of in flight at once:
+  // a CTA's 4,096 of them took about 7,000 cycles
+  const bool q_by_map = !E4M3 && q_tma && it.direct_rows;
 
   if (threadIdx.x == 0) {
     // e4m3: a K / V stage is filled by the two converter warps' arrivals
@@ -211,6 +218,7 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(mma_drain, 1);
+    mbar_init(q_full, 1);
     fence_mbar_init();
   }
 
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
         const uint4 w = e_row[k] >= 0 ? bf16x8_to_f16x8(e_val[k]) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(smem + C::kOffQ + t * C::kQTile + panel * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = w;
       }
-    } else {
+    } else if (!q_by_map) {
       int src_row[kPer];
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
@@ -421,11 +429,22 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     // overwrites P_t(j-1)).  A K (V) stage is released by a commit after the
     // last S (PV) that reads it.  (Issuing S first measured the same.)
     if (lane == 0) {
+      uint32_t idle = 0;
+      if (q_by_map) {
+        // box: d 64 x G heads x 128/G rows = one 128-row panel of one Q tile;
+        // rows past M bring later rows' Q (or zeros past the batch's last
+        // row), whose results are dropped
+        mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(n_qt * C::kQTile));
+        for (int t = 0; t < n_qt; ++t)
+          for (int panel = 0; panel < C::kPanels; ++panel)
+            tma_load_3d(smem + C::kOffQ + t * C::kQTile + panel * 16384, &q_map, 64 * panel, head * G,
+                        it.rows_off + t * (128 / G), q_full);
+        if (!mbar_wait(q_full, 0, err)) idle = kWaitLimit;
+      }
       const uint32_t id_s = tc::idesc_f16kind(128, C::kKeys, false, false, !E4M3);
       const uint32_t id_o = tc::idesc_f16kind(128, D, false, true, !E4M3);
       int s_next[2] = {0, n_qt > 1 ? 0 : nkv};
       int pv_next[2] = {0, n_qt > 1 ? 0 : nkv};
-      uint32_t idle = 0;
       while ((pv_next[0] < nkv || pv_next[1] < nkv) && idle < kWaitLimit) {
         bool progressed = false;
         for (int t = 0; t < n_qt; ++t) {
@@ -672,16 +691,18 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
 }
 
 template <int D, bool E4M3, bool CAP>
-cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
-                     const void* vpool, const float* kscale, const float* vscale, void* out, float* lse, float* acc,
-                     float* ml, int* err, cudaStream_t st) {
+cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void* q, const CUtensorMap* q_map,
+                     const void* kpool, const void* vpool, const float* kscale, const float* vscale, void* out,
+                     float* lse, float* acc, float* ml, int* err, cudaStream_t st) {
   using C = PreCfg<D, E4M3>;
   static_assert(C::kSmem <= 227 * 1024, "shared memory budget");
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, E4M3, CAP>>(C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_pre, g.hkv);
+  const CUtensorMap no_map{};
   e = launch_pdl(prefill_kernel<D, E4M3, CAP>, grid, C::kThreads, C::kSmem, st, g, p, layer,
-                 static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(kpool),
+                 static_cast<const __nv_bfloat16*>(q), q_map ? *q_map : no_map, q_map ? 1 : 0,
+                 static_cast<const uint8_t*>(kpool),
                  static_cast<const uint8_t*>(vpool), kscale, vscale, static_cast<__nv_bfloat16*>(out), lse, acc, ml,
                  err);
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -689,12 +710,12 @@ cudaError_t launch_t(const Geometry& g, const PlanView& p, int layer, const void
 
 }  // namespace
 
-cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, const void* q, const void* kpool,
-                           const void* vpool, const float* scale_k, const float* scale_v, void* out, float* lse,
-                           float* part_acc, float* part_ml, int* err, cudaStream_t st) {
+cudaError_t launch_prefill(const Geometry& g, const PlanView& p, int layer, const void* q, const CUtensorMap* q_map,
+                           const void* kpool, const void* vpool, const float* scale_k, const float* scale_v,
+                           void* out, float* lse, float* part_acc, float* part_ml, int* err, cudaStream_t st) {
   if (p.n_pre == 0) return cudaSuccess;
 #define PIE_PREFILL(DD, E, CP) \
-  launch_t<DD, E, CP>(g, p, layer, q, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st)
+  launch_t<DD, E, CP>(g, p, layer, q, q_map, kpool, vpool, scale_k, scale_v, out, lse, part_acc, part_ml, err, st)
   const bool cap = g.softcap > 0.f;
   if (g.kv_dtype != 0) {
     if (g.d != 128) return cudaErrorInvalidValue;

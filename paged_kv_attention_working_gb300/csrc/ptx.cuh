@@ -83,6 +83,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Tiled 3-D tensor copy global -> shared through a tensor map (a kernel
+// parameter), completion counted on an mbarrier.  (x, y, z) is the box's
+// first element; x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (no register staging); both
 // addresses 16-byte aligned.  Completed by cp_async_wait_all.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
