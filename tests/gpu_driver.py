@@ -14,7 +14,7 @@ def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
 
 
 class DeviceRun:
-    def __init__(self, w, device="cuda"):
+    def __init__(self, w, device="cuda", num_sms=0):
         self.w = w
         esize = 2 if w.kv_dtype == pie.PIE_KV_BF16 else 1
         self.block = 16 * w.head_dim * esize
@@ -27,7 +27,8 @@ class DeviceRun:
                                       kv_dtype=w.kv_dtype, free_list=w.free_list().tolist(), k_scale=ks,
                                       v_scale=vs, k_pool=self.kpool, v_pool=self.vpool,
                                       stream=self.stream.cuda_stream, logit_softcap=w.logit_softcap,
-                                      rope_theta=w.rope_theta, rope_max_positions=w.rope_positions)
+                                      rope_theta=w.rope_theta, rope_max_positions=w.rope_positions,
+                                      num_sms=num_sms)
         self.handles = {}
 
     def run(self, layers=None, kv_source=None):

@@ -39,11 +39,10 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("name", list(wl.FULL) + list(wl.EXTRA))
-def test_reduced_workload_parity(name):
+def _parity(name, num_sms=0):
     w = wl.reduced(name)
     store, handles, ref_passes = oracle_driver.run(w)
-    g = gpu_driver.DeviceRun(w)
+    g = gpu_driver.DeviceRun(w, num_sms=num_sms)
     passes = g.run()
     kp, vp = g.pools()
     np.testing.assert_array_equal(kp, store.pool[0])
@@ -58,6 +57,23 @@ def test_reduced_workload_parity(name):
             lse = got["lse"][layer].cpu().numpy()
             assert_close(lse, ref["lse"][layer], LSE_ATOL, 0.0, f"{name} lse layer {layer}")
     g.close()
+
+
+@pytest.mark.parametrize("name", list(wl.FULL) + list(wl.EXTRA))
+def test_reduced_workload_parity(name):
+    _parity(name)
+
+
+# A context planned for 2 SMs: every tensor-core launch then runs more than
+# one wave, so items whose rows are in batch order load their Q tiles by
+# tensor copies, with each head shape's box (d 64 x G heads x 128/G rows);
+# the decode items take the plan's fewer KV splits.
+@pytest.mark.parametrize("name", ["mixed_batch", "mixed_batch_e4m3", "mixed_batch_d64", "mixed_batch_mha",
+                                  "mixed_batch_g8", "mixed_batch_g16", "mixed_batch_mqa_g32", "mixed_batch_mqa_g64",
+                                  "mixed_batch_d64_mqa_g16", "mixed_batch_softcap", "fork_spec", "edge_batch",
+                                  "interleaved_forks"])
+def test_reduced_workload_parity_few_sms(name):
+    _parity(name, num_sms=2)
 
 
 @pytest.mark.parametrize("scale", [5.0 / 448.0, 0.37, 1.0])
