@@ -64,10 +64,9 @@ def test_reduced_workload_parity(name):
     _parity(name)
 
 
-# A context planned for 2 SMs: every tensor-core launch then runs more than
-# one wave, so items whose rows are in batch order load their Q tiles by
-# tensor copies, with each head shape's box (d 64 x G heads x 128/G rows);
-# the decode items take the plan's fewer KV splits.
+# A context planned for 2 SMs: the planner then splits the KV runs far less
+# (decode items of many more pages, shared runs in one item per row tile),
+# and every tensor-core launch spans several waves.
 @pytest.mark.parametrize("name", ["mixed_batch", "mixed_batch_e4m3", "mixed_batch_d64", "mixed_batch_mha",
                                   "mixed_batch_g8", "mixed_batch_g16", "mixed_batch_mqa_g32", "mixed_batch_mqa_g64",
                                   "mixed_batch_d64_mqa_g16", "mixed_batch_softcap", "fork_spec", "edge_batch",
