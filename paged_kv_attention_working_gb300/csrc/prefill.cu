@@ -29,8 +29,11 @@
 //                   writes P back as bf16 pairs over the row's first 64 S
 //                   columns.
 // Tensor memory: S/P of tile t at columns t*128, O of tile t at 256 + t*d.
-// Rows with one part are normalised and written as bf16; otherwise the
-// fp32 (acc, m, l) partial goes to the merge kernel.
+// Q tiles: items whose rows are in batch order take them by tensor copies
+// (one box of a 3-D map over [rows][Hq][d] per 64-column panel), the others
+// by the softmax warps' cp.async copies.  Rows with one part are normalised
+// and written as bf16; otherwise the fp32 (acc, m, l) partial goes to the
+// merge kernel; either way through the tile's Q buffer, whole rows per store.
 //
 // With a logit soft cap c (CAP), the softmax warps map each raw score to
 // tanh(s * scale / c) before masking, and c * log2(e) takes the place of the
