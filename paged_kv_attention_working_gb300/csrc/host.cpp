@@ -968,8 +968,8 @@ pie_status pie_kv_append_rope(pie_ctx* c, pie_batch* b, int32_t layer, const voi
   return PIE_OK;
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library); null when the driver does not offer it.
+// cuTensorMapEncodeTiled through the CUDA runtime's driver entry point (no link
+// against the CUDA driver library); null when the driver does not offer it.
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
