@@ -458,12 +458,12 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
             const uint32_t vaddr = sbase + C::kOffV + (j % C::kVStages) * C::kKVTile;
             const uint32_t p_tmem = tmem + t * C::kKeys;  // 16 keys = 8 columns per k-step
             const uint32_t d_o = tmem + C::kColO + t * D;
+            const uint32_t v_lo = tc::sw128_lo(vaddr, E4M3 ? C::kPanelBytes : 2048);
+            constexpr uint32_t v_hi = tc::sw128_hi(1024);
 #pragma unroll
             for (int ks = 0; ks < C::kKeys / 16; ++ks)
-              tc::mma_bf16_ts(d_o, p_tmem + ks * 8,
-                              E4M3 ? tc::sw128_desc(vaddr + ks * 2048, C::kPanelBytes, 1024)
-                                   : tc::sw128_desc(vaddr + ks * (16 * D * 2), 2048, 1024),
-                              id_o, j > 0 || ks > 0);
+              tc::mma_bf16_ts_w(d_o, p_tmem + ks * 8, v_lo + ((E4M3 ? ks * 2048 : ks * (16 * D * 2)) >> 4), v_hi,
+                                id_o, j > 0 || ks > 0);
             tc::commit(&o_done[t]);
             pv_next[t] = j + 1;
             if (pv_next[1 - t] > j) tc::commit(&v_empty[j % C::kVStages]);
@@ -478,12 +478,13 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
             const uint32_t kaddr = sbase + C::kOffK + (j % C::kKStages) * C::kKVTile;
             const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
             const uint32_t d_s = tmem + t * C::kKeys;
+            const uint32_t q_lo = tc::sw128_lo(qaddr, 16), k_lo = tc::sw128_lo(kaddr, 16);
+            constexpr uint32_t qk_hi = tc::sw128_hi(1024);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
               const uint32_t off_q = (ks >> 2) * 16384 + (ks & 3) * 32;
               const uint32_t off_k = (ks >> 2) * C::kPanelBytes + (ks & 3) * 32;
-              tc::mma_bf16(d_s, tc::sw128_desc(qaddr + off_q, 16, 1024), tc::sw128_desc(kaddr + off_k, 16, 1024),
-                           id_s, ks > 0);
+              tc::mma_bf16_w(d_s, q_lo + (off_q >> 4), qk_hi, k_lo + (off_k >> 4), qk_hi, id_s, ks > 0);
             }
             tc::commit(&s_full[t]);
             s_next[t] = j + 1;
