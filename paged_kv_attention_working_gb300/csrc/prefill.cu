@@ -446,16 +446,21 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
       }
       const uint32_t id_s = tc::idesc_f16kind(128, C::kKeys, false, false, !E4M3);
       const uint32_t id_o = tc::idesc_f16kind(128, D, false, true, !E4M3);
+      // Per tile: the next S and PV, and the K / V ring stage and phase they
+      // read; the tile loops are unrolled so that all of it stays in
+      // registers (the thread's instruction count paces every hand-off).
       int s_next[2] = {0, n_qt > 1 ? 0 : nkv};
       int pv_next[2] = {0, n_qt > 1 ? 0 : nkv};
+      int k_st[2] = {0, 0}, v_st[2] = {0, 0};
+      uint32_t k_ph[2] = {0, 0}, v_ph[2] = {0, 0};
       while ((pv_next[0] < nkv || pv_next[1] < nkv) && idle < kWaitLimit) {
         bool progressed = false;
-        for (int t = 0; t < n_qt; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
           const int j = pv_next[t];
-          if (j < s_next[t] && mbar_test_wait(&p_full[t], j & 1) &&
-              mbar_test_wait(&v_full[j % C::kVStages], (j / C::kVStages) & 1)) {
+          if (j < s_next[t] && mbar_test_wait(&p_full[t], j & 1) && mbar_test_wait(&v_full[v_st[t]], v_ph[t])) {
             tc::fence_after();
-            const uint32_t vaddr = sbase + C::kOffV + (j % C::kVStages) * C::kKVTile;
+            const uint32_t vaddr = sbase + C::kOffV + v_st[t] * C::kKVTile;
             const uint32_t p_tmem = tmem + t * C::kKeys;  // 16 keys = 8 columns per k-step
             const uint32_t d_o = tmem + C::kColO + t * D;
             const uint32_t v_lo = tc::sw128_lo(vaddr, E4M3 ? C::kPanelBytes : 2048);
@@ -466,16 +471,21 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
                                 id_o, j > 0 || ks > 0);
             tc::commit(&o_done[t]);
             pv_next[t] = j + 1;
-            if (pv_next[1 - t] > j) tc::commit(&v_empty[j % C::kVStages]);
+            if (pv_next[1 - t] > j) tc::commit(&v_empty[v_st[t]]);
+            if (++v_st[t] == C::kVStages) {
+              v_st[t] = 0;
+              v_ph[t] ^= 1u;
+            }
             progressed = true;
           }
         }
-        for (int t = 0; t < n_qt; ++t) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
           const int j = s_next[t];
-          if (j < nkv && pv_next[t] == j && mbar_test_wait(&k_full[j % C::kKStages], (j / C::kKStages) & 1) &&
+          if (j < nkv && pv_next[t] == j && mbar_test_wait(&k_full[k_st[t]], k_ph[t]) &&
               (j == 0 || mbar_test_wait(&o_done[t], (j - 1) & 1))) {
             tc::fence_after();
-            const uint32_t kaddr = sbase + C::kOffK + (j % C::kKStages) * C::kKVTile;
+            const uint32_t kaddr = sbase + C::kOffK + k_st[t] * C::kKVTile;
             const uint32_t qaddr = sbase + C::kOffQ + t * C::kQTile;
             const uint32_t d_s = tmem + t * C::kKeys;
             const uint32_t q_lo = tc::sw128_lo(qaddr, 16), k_lo = tc::sw128_lo(kaddr, 16);
@@ -488,7 +498,11 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
             }
             tc::commit(&s_full[t]);
             s_next[t] = j + 1;
-            if (s_next[1 - t] > j) tc::commit(&k_empty[j % C::kKStages]);
+            if (s_next[1 - t] > j) tc::commit(&k_empty[k_st[t]]);
+            if (++k_st[t] == C::kKStages) {
+              k_st[t] = 0;
+              k_ph[t] ^= 1u;
+            }
             progressed = true;
           }
         }
