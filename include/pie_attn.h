@@ -25,6 +25,11 @@
  *    stream-ordered use on the context's stream; no call synchronises that
  *    stream except where stated (pie_ctx_destroy, buffer growth in
  *    pie_batch_begin).
+ *  - Device pools, K, V, Q and output arrays must be 16-byte aligned (any
+ *    CUDA allocation is, and so is every row of a contiguous [rows][heads][d]
+ *    array); LSE arrays, block tables and row lengths 4-byte aligned.  The
+ *    kernels move them in 16-byte vectors and bulk copies; a call given a
+ *    misaligned pointer returns PIE_ERR_INVALID and launches nothing.
  *  - All device work of a context is ordered on its stream, in call order
  *    (pie_attend may run part of a pass on a second stream the context owns,
  *    forked from and joined back into that stream within the call).  The

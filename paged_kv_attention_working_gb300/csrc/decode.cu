@@ -722,6 +722,12 @@ extern "C" pie_status pie_attend_decode_noalloc(const pie_decode_args* a) {
   if (static_cast<int64_t>(R) * a->max_pages_per_row >= (int64_t{1} << 31)) return PIE_ERR_RANGE;
   if (R == 0) return PIE_OK;
   if (!a->q || !a->k_pool || !a->v_pool || !a->block_table || !a->seq_lens || !a->out) return PIE_ERR_INVALID;
+  {
+    auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+    if (!al(a->q, 16) || !al(a->k_pool, 16) || !al(a->v_pool, 16) || !al(a->out, 16) || !al(a->block_table, 4) ||
+        !al(a->seq_lens, 4) || !al(a->lse, 4))
+      return PIE_ERR_INVALID;
+  }
   if (noalloc_layout(R, 1, hq, d).total > kNoAllocBytes) return PIE_ERR_RANGE;
 
   int dev = 0, sms = 0;

@@ -121,6 +121,11 @@ struct pie_ctx {
 
 namespace {
 
+// Device pointers the kernels read or write with 16-byte (or 4-byte) vector
+// accesses and bulk copies must be aligned to that; null passes (its own
+// checks come later).
+bool aligned(const void* p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0; }
+
 pie_status fail(pie_ctx* c, pie_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -512,6 +517,7 @@ pie_status pie_ctx_create(const pie_config* cfg, pie_ctx** out) {
                 (k.kv_dtype == PIE_KV_E4M3 && k.head_dim == 128);
   if (!dim_ok || G > 64 || (G & (G - 1))) return PIE_ERR_INVALID;
   if ((k.k_pool == nullptr) != (k.v_pool == nullptr)) return PIE_ERR_INVALID;
+  if (!aligned(k.k_pool, 16) || !aligned(k.v_pool, 16)) return PIE_ERR_INVALID;
   if (k.kv_dtype == PIE_KV_E4M3 && (!k.k_scale || !k.v_scale)) return PIE_ERR_INVALID;
   if (!(k.logit_softcap >= 0.0f) || !std::isfinite(k.logit_softcap)) return PIE_ERR_INVALID;
   if (!(k.rope_theta >= 0.0f) || !std::isfinite(k.rope_theta)) return PIE_ERR_INVALID;
@@ -921,6 +927,7 @@ pie_status pie_batch_slots(const pie_batch* b, int32_t* pos, int32_t* slot) {
 
 pie_status pie_kv_append(pie_ctx* c, pie_batch* b, int32_t layer, const void* k, const void* v) {
   if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(c, PIE_ERR_INVALID, "K or V not 16-byte aligned");
   if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
   if (layer < 0 || layer >= c->geo.num_layers) return fail(c, PIE_ERR_INVALID, "layer %d", layer);
   if (b->n_rows == 0) return PIE_OK;
@@ -951,6 +958,8 @@ pie_status pie_rope_table(float theta, int32_t head_dim, int32_t positions, floa
 pie_status pie_kv_append_rope(pie_ctx* c, pie_batch* b, int32_t layer, const void* k, const void* v, const void* q,
                               void* q_out) {
   if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q, 16) || !aligned(q_out, 16))
+    return fail(c, PIE_ERR_INVALID, "K, V, Q or the rotated Q not 16-byte aligned");
   if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
   if (!c->d_rope) return fail(c, PIE_ERR_STATE, "context has no rotary table (rope_theta = 0)");
   if (layer < 0 || layer >= c->geo.num_layers) return fail(c, PIE_ERR_INVALID, "layer %d", layer);
@@ -1012,6 +1021,8 @@ static bool q_tensor_map(pie_ctx* c, const void* q, int32_t n_rows, CUtensorMap*
 
 pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, void* out, float* lse) {
   if (!c || !b || b != c->open) return c ? fail(c, PIE_ERR_BAD_HANDLE, "not the open batch") : PIE_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return fail(c, PIE_ERR_INVALID, "Q or output not 16-byte aligned, or LSE not 4-byte aligned");
   if (c->plan_only) return fail(c, PIE_ERR_STATE, "plan-only context");
   if (layer < 0 || layer >= c->geo.num_layers) return fail(c, PIE_ERR_INVALID, "layer %d", layer);
   if (b->n_rows == 0) return PIE_OK;

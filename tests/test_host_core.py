@@ -414,7 +414,7 @@ def test_rope_append_on_a_plan_only_context_is_a_state_error():
     h = pie.pie_ws_create(c)
     b = pie.pie_batch_begin(c, [(h, 21, None)])
     with pytest.raises(pie.PieError) as e:
-        pie.pie_kv_append_rope(c, b, 0, 1, 1)
+        pie.pie_kv_append_rope(c, b, 0, 16, 16)   # aligned stand-ins, never dereferenced
     assert e.value.status == pie.PIE_ERR_STATE
     pie.pie_batch_end(c, b)
     pie.pie_ctx_destroy(c)
@@ -462,3 +462,25 @@ def test_plan_marks_consecutive_rows_direct():
                 assert it["direct_rows"] == 1 and it["rows_off"] % 3 == 0
         pie.pie_batch_end(c, b)
         pie.pie_ctx_destroy(c)
+
+
+def test_misaligned_pointers_are_rejected_before_any_launch():
+    """K, V, Q and outputs move in 16-byte vectors and bulk copies: a call
+    given a misaligned pointer fails with PIE_ERR_INVALID before it checks
+    anything that would need a GPU (here a plan-only context, whose
+    well-aligned calls fail with PIE_ERR_STATE instead)."""
+    import ctypes
+    c = pie.pie_ctx_create(1, 8, 2, 64, 16)
+    ws = pie.pie_ws_create(c)
+    b = pie.pie_batch_begin(c, [(ws, 3, None)])
+    lib = pie.lib
+    odd, ok = 0x1008, 0x1000          # never dereferenced: the calls return first
+    assert lib.pie_attend(c, b, 0, odd, ok, None) == pie.PIE_ERR_INVALID
+    assert lib.pie_attend(c, b, 0, ok, odd, None) == pie.PIE_ERR_INVALID
+    assert lib.pie_attend(c, b, 0, ok, ok, ctypes.c_void_p(0x1002)) == pie.PIE_ERR_INVALID
+    assert lib.pie_attend(c, b, 0, ok, ok, None) == pie.PIE_ERR_STATE
+    assert lib.pie_kv_append(c, b, 0, odd, ok) == pie.PIE_ERR_INVALID
+    assert lib.pie_kv_append(c, b, 0, ok, ok) == pie.PIE_ERR_STATE
+    assert lib.pie_kv_append_rope(c, b, 0, ok, ok, odd, ok) == pie.PIE_ERR_INVALID
+    pie.pie_batch_end(c, b)
+    pie.pie_ctx_destroy(c)
