@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(PreCfg<D, E4M3>::kThreads, 1)
     fence_mbar_init();
   }
 
-  // Q tiles -> shared memory, 128-byte swizzled K-major, rows past M zero;
-  // loaded by the softmax warps while the producers already fetch K and V.
+  // Q tiles that do not come by tensor copies -> shared memory, 128-byte
+  // swizzled K-major, rows past M zero; loaded by the softmax warps while the
+  // producers already fetch K and V.
   // Every load of a thread is in flight at once (16-byte cp.async copies,
   // or, for e4m3 contexts, register loads for the f16 conversion, issued
   // before the barriers and tensor memory are set up); a load loop that
