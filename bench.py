@@ -337,6 +337,7 @@ def run_gpu(args, w, world, rank, local, e2e=True):
                              k_scale=ks, v_scale=vs, k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream,
                              logit_softcap=args.logit_softcap, rope_theta=args.rope_theta,
                              rope_max_positions=(max(w.ctx) + 2) if args.rope_theta else 0)
+    pie.pie_ctx_set_merge_mode(ctx, args.merge_mode)
     # set-up: every operation of the workload before its final (decode) pass,
     # with random bf16 K/V generated on the device
     gen = torch.Generator(device=dev)
@@ -469,7 +470,7 @@ def run_gpu(args, w, world, rank, local, e2e=True):
     achieved = attend_bytes / (attend_avg * 1e-3) / 1e9
     # append, tensor-core items, narrow and wide decode items, merge
     launches_per_layer = (1 + (info["prefill_items"] > 0) + (info["decode_items"] > info["wide_decode_items"])
-                          + (info["wide_decode_items"] > 0) + (info["merge_rows"] > 0))
+                          + (info["wide_decode_items"] > 0) + info["merge_launch"])
     result = {
         "metric": "decode attend KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -480,7 +481,7 @@ def run_gpu(args, w, world, rank, local, e2e=True):
                    "hq": Hq, "hkv": Hkv, "head_dim": D, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
                    "page_size": 16, "l2": "inputs larger than L2 (~1.1 GB KV per layer)",
                    "logit_softcap": args.logit_softcap, "rope_theta": args.rope_theta,
-                   "parallelism": f"replicas x{world}"},
+                   "merge_mode": args.merge_mode, "parallelism": f"replicas x{world}"},
         "rows_per_s": world * n_rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
                      "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
@@ -521,6 +522,7 @@ def run_fork(args, world, rank, local):
     vpool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
     ctx = pie.pie_ctx_create(L, Hq, Hkv, D, w.num_pages, free_list=w.free_list().tolist(), k_pool=kpool,
                              v_pool=vpool, stream=stream.cuda_stream, logit_softcap=args.logit_softcap)
+    pie.pie_ctx_set_merge_mode(ctx, args.merge_mode)
     gen = torch.Generator(device=dev)
     gen.manual_seed(3000 + rank)
     hs = {}
@@ -639,6 +641,7 @@ def run_mixed(args, w, world, rank, local):
                              free_list=w.free_list().tolist(), k_scale=ks, v_scale=vs,
                              k_pool=kpool, v_pool=vpool, stream=stream.cuda_stream,
                              logit_softcap=args.logit_softcap)
+    pie.pie_ctx_set_merge_mode(ctx, args.merge_mode)
     gen = torch.Generator(device=dev)
     gen.manual_seed(2000 + rank)
     hs = {}
@@ -780,6 +783,9 @@ def main():
                     help="rotary base: K and Q rotated in the append (pie_kv_append_rope); 0 = plain append")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers of the workload (32 = the full Llama-3.1-8B shape; fewer only for profiling)")
+    ap.add_argument("--merge-mode", type=int, default=0, choices=[0, 1],
+                    help="how split rows are combined (pie_ctx_set_merge_mode): 0 = a merge launch, "
+                         "1 = inside the decode launches when no tensor-core item is split")
     ap.add_argument("--only-headline", action="store_true",
                     help="time the headline workload alone (no fork / mixed / 70B sub-objects)")
     args = ap.parse_args()

@@ -248,9 +248,27 @@ pie_status pie_rope_table(float theta, int32_t head_dim, int32_t positions, floa
  * its scale); scores and sums are fp32; the softmax weights meet V as bf16
  * (bf16 pools) or f16 (e4m3 pools).  With an e4m3 pool, rows that take the
  * tensor-core path (prefill chunks, large fork groups) also round q to f16,
- * so |q| must stay below 65504 there. */
+ * so |q| must stay below 65504 there.
+ * Rows whose keys are split over several work items are combined from the
+ * parts' (max, sum, partial output) as in "How Pie thinks", section 4 (the
+ * shared prefix is attended once and its result combined with each
+ * member's own pages): by the decode kernels themselves, the CTA that
+ * stores a row's last part combining them (see pie_ctx_set_merge_mode),
+ * or by a merge launch after the attention launches. */
 pie_status pie_attend(pie_ctx* ctx, pie_batch* b, int32_t layer,
                       const void* q, void* out, float* lse);
+/* How pie_attend combines split rows (the combination of partial results
+ * under pie_attend, "How Pie thinks", section 4), for batches begun after
+ * the call.  mode 0 (the default): a merge launch after the attention
+ * launches.  mode 1: inside the decode launches, one launch per pie_attend,
+ * when no tensor-core item of the batch is split (else a merge launch).
+ * Merging inside holds each split CTA a few microseconds longer, to publish
+ * its stores and count them; on one GB300, both modes in the same run, that
+ * cost more than the merge launch: 2.1 % on a decode batch of 64 rows of
+ * 32 q / 8 KV heads (2.9 MB of partials) and 1.4 % on one of 256 rows of
+ * 64 q / 8 KV heads over e4m3 pages (23 MB).  PIE_ERR_INVALID for another
+ * mode. */
+pie_status pie_ctx_set_merge_mode(pie_ctx* ctx, int32_t mode);
 /* Closes the batch.  Its device work stays enqueued on the stream. */
 pie_status pie_batch_end(pie_ctx* ctx, pie_batch* b);
 
@@ -313,8 +331,10 @@ typedef struct pie_decode_args {
 pie_status pie_attend_decode_noalloc(const pie_decode_args* args);
 
 /* ---- introspection (tests, tools) ---- */
-/* info[0..3] = decode-kernel items, tensor-core items, rows merged from
- * several partial results, copy-on-write page copies. */
+/* info[0..4] = decode-kernel items, tensor-core items, rows merged from
+ * several partial results, copy-on-write page copies, and 1 when each
+ * pie_attend of the batch ends with a merge launch, 0 when the decode
+ * kernels merge the split rows themselves or no row is split. */
 pie_status pie_batch_plan_info(const pie_batch* b, int32_t* info);
 /* Copies work items (kind 0: decode kernel, 1: tensor-core kernel), 8 int32
  * each: first page index into the batch's page list, pages, first key

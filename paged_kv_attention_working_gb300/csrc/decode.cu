@@ -63,6 +63,137 @@ struct DecodeCfg {
   static constexpr int kSmem = (kRing > kCombineFloats * 4 ? kRing : kCombineFloats * 4) + 2 * kStages * 8 + 16;
 };
 
+// One warp combines the np parts (m_i, l_i, acc_i) of (row, query head qh),
+// stored from part index base on, in the log2 domain:
+//   m = max m_i,  l = sum l_i 2^(m_i - m),  o = sum acc_i 2^(m_i - m) / l,
+// and writes o (bf16) and the LSE.  Lane k holds part k's (m, l) (32 parts
+// at a time), so the parts' loads are issued together; the weights reach
+// every lane by shuffle, and each lane accumulates E dims of the parts'
+// partial outputs with vector loads (the first eight issued with the (m, l)
+// loads, the rest four at a time).  The loads bypass L1: inside a decode
+// launch the parts were written by other CTAs moments earlier.
+template <int D>
+__device__ __forceinline__ void merge_parts(const Geometry& g, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                            const float* __restrict__ part_acc, const float* __restrict__ part_ml,
+                                            int row, int np, int base, int qh, int lane) {
+  auto ml_at = [&](int k) {
+    return k < np ? __ldcg(reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(base + k) * g.hq + qh) * 2))
+                  : make_float2(-INFINITY, 0.f);
+  };
+  constexpr int E = D / 32;
+  using Vec = typename std::conditional<E == 4, float4, float2>::type;
+  const float* a = part_acc + (static_cast<int64_t>(base) * g.hq + qh) * D + lane * E;
+  const int64_t part_stride = static_cast<int64_t>(g.hq) * D;
+  // The first kPre parts' partial outputs are loaded together with the (m, l)
+  // values (they do not depend on the weights): one round trip to L2 fewer
+  // before the sums, which is most of this kernel's time in a small pass.
+  constexpr int kPre = 8;
+  Vec pre[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    if (k < np) {
+      pre[k] = __ldcg(reinterpret_cast<const Vec*>(a + k * part_stride));
+    } else {
+      reinterpret_cast<float*>(&pre[k])[0] = 0.f;
+      reinterpret_cast<float*>(&pre[k])[1] = 0.f;
+      if constexpr (E == 4) {
+        reinterpret_cast<float*>(&pre[k])[2] = 0.f;
+        reinterpret_cast<float*>(&pre[k])[3] = 0.f;
+      }
+    }
+  }
+  const float2 ml0 = ml_at(lane);
+  float m = ml0.x;
+  for (int k0 = 32; k0 < np; k0 += 32) m = fmaxf(m, ml_at(k0 + lane).x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float base_m = m == -INFINITY ? 0.f : m;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  auto add = [&](const Vec& v, float wk) {
+    acc[0] += v.x * wk;
+    acc[1] += v.y * wk;
+    if constexpr (E == 4) {
+      acc[2] += reinterpret_cast<const float4&>(v).z * wk;
+      acc[3] += reinterpret_cast<const float4&>(v).w * wk;
+    }
+  };
+  float l = 0.f;
+  for (int k0 = 0; k0 < np; k0 += 32) {
+    const float2 ml = k0 == 0 ? ml0 : ml_at(k0 + lane);
+    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - base_m);
+    l += ml.y * w;
+    const int n = min(32, np - k0);
+    if (k0 == 0) {
+#pragma unroll
+      for (int kk = 0; kk < kPre; ++kk) add(pre[kk], __shfl_sync(0xffffffffu, w, kk));
+    }
+    const int first = k0 == 0 ? kPre : 0;
+#pragma unroll 4
+    for (int kk = first; kk < n; ++kk)
+      add(__ldcg(reinterpret_cast<const Vec*>(a + (k0 + kk) * part_stride)), __shfl_sync(0xffffffffu, w, kk));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D + lane * E;
+  if constexpr (E == 4) {
+    uint2 wv;
+    wv.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    wv.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = wv;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  }
+  if (lse && lane == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (m + __log2f(l)) * 0.6931471805599453f;
+}
+
+// Merge inside the attention launch: a warp has just stored its partial
+// results for the columns (colrow[e], colqh[e]) of one N tile (the 8 lanes
+// of one tq hold the same two columns).  Each (row, query head) has a
+// counter of the parts stored so far; one lane per column counts its part,
+// and the warp that stores a column's last part resets the counter and
+// combines the column's parts at once, so no separate merge launch follows.
+// Each column lies in one warp's N tile per CTA, and each of the row's parts
+// is one CTA, so the count reaches the row's number of parts exactly once.
+template <int D>
+__device__ __forceinline__ void count_and_merge(const Geometry& g, const PlanView& p, __nv_bfloat16* out, float* lse,
+                                                const float* part_acc, const float* part_ml, const int (&colrow)[2],
+                                                const int (&colqh)[2], int gq, int lane) {
+  __threadfence();  // this lane's partial stores, before the count
+  __syncwarp();
+  uint32_t last = 0;
+  if (gq == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (colrow[e] < 0) continue;
+      const int i = p.row_merge[colrow[e]];
+      int* cnt = p.merge_cnt + static_cast<int64_t>(i) * g.hq + colqh[e];
+      if (atomicAdd(cnt, 1) == p.merge_info[i].y - 1) {
+        *cnt = 0;  // every part is counted: the next launch starts from zero
+        last |= 1u << e;
+      }
+    }
+  }
+  __threadfence();  // the other parts' stores, before the loads of the merge
+  __syncwarp();
+  uint32_t todo = __ballot_sync(0xffffffffu, last != 0);
+  while (todo) {
+    const int src = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const uint32_t cols = __shfl_sync(0xffffffffu, last, src);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = __shfl_sync(0xffffffffu, colrow[e], src), qh = __shfl_sync(0xffffffffu, colqh[e], src);
+      if (cols >> e & 1u) {
+        const int4 mi = p.merge_info[p.row_merge[row]];
+        merge_parts<D>(g, out, lse, part_acc, part_ml, row, mi.y, mi.z, qh, lane);
+      }
+    }
+  }
+}
+
 template <bool E4M3, int D, bool CAP, int NTW>
 __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geometry g, PlanView p, int layer,
                                                           const __nv_bfloat16* __restrict__ q,
@@ -465,99 +596,22 @@ __global__ void __launch_bounds__(kThreads, NTW == 1 ? 4 : 3) decode_kernel(Geom
         }
         if (gq == 0) *reinterpret_cast<float2*>(part_ml + slot * 2) = make_float2(mx[i][e], sum[i][e]);
       }
+      if (p.merge_cnt) count_and_merge<D>(g, p, out, lse, part_acc, part_ml, colrow, colqh, gq, lane);
     }
   }
 }
 
-// One warp per (merged row, query head): combine the row's parts
-// (m_i, l_i, acc_i) in the log2 domain:
-//   m = max m_i,  l = sum l_i 2^(m_i - m),  o = sum acc_i 2^(m_i - m) / l.
+// One warp per (merged row, query head): the separate merge launch, for
+// passes whose split rows are not merged inside the attention kernels.
 template <int D>
 __global__ void merge_kernel(Geometry g, PlanView p, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                              const float* __restrict__ part_acc, const float* __restrict__ part_ml) {
-  // One warp per (merged row, query head).  Lane k holds part k's (m, l)
-  // (32 parts at a time), so the parts' loads are issued together; the
-  // weights reach every lane by shuffle, and each lane accumulates E dims of
-  // the parts' partial outputs with vector loads (the first eight issued
-  // with the (m, l) loads, the rest four at a time).
   pdl_wait();
   pdl_trigger();
   int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.n_merge * g.hq) return;
-  int i = wid / g.hq, qh = wid % g.hq;
-  const int4 mi = p.merge_info[i];  // one load: (row, parts, first part)
-  const int row = mi.x, np = mi.y, base = mi.z;
-  auto ml_at = [&](int k) {
-    return k < np ? *reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(base + k) * g.hq + qh) * 2)
-                  : make_float2(-INFINITY, 0.f);
-  };
-  constexpr int E = D / 32;
-  using Vec = typename std::conditional<E == 4, float4, float2>::type;
-  const float* a = part_acc + (static_cast<int64_t>(base) * g.hq + qh) * D + lane * E;
-  const int64_t part_stride = static_cast<int64_t>(g.hq) * D;
-  // The first kPre parts' partial outputs are loaded together with the (m, l)
-  // values (they do not depend on the weights): one round trip to L2 fewer
-  // before the sums, which is most of this kernel's time in a small pass.
-  constexpr int kPre = 8;
-  Vec pre[kPre];
-#pragma unroll
-  for (int k = 0; k < kPre; ++k) {
-    if (k < np) {
-      pre[k] = *reinterpret_cast<const Vec*>(a + k * part_stride);
-    } else {
-      reinterpret_cast<float*>(&pre[k])[0] = 0.f;
-      reinterpret_cast<float*>(&pre[k])[1] = 0.f;
-      if constexpr (E == 4) {
-        reinterpret_cast<float*>(&pre[k])[2] = 0.f;
-        reinterpret_cast<float*>(&pre[k])[3] = 0.f;
-      }
-    }
-  }
-  const float2 ml0 = ml_at(lane);
-  float m = ml0.x;
-  for (int k0 = 32; k0 < np; k0 += 32) m = fmaxf(m, ml_at(k0 + lane).x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const float base_m = m == -INFINITY ? 0.f : m;
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  auto add = [&](const Vec& v, float wk) {
-    acc[0] += v.x * wk;
-    acc[1] += v.y * wk;
-    if constexpr (E == 4) {
-      acc[2] += reinterpret_cast<const float4&>(v).z * wk;
-      acc[3] += reinterpret_cast<const float4&>(v).w * wk;
-    }
-  };
-  float l = 0.f;
-  for (int k0 = 0; k0 < np; k0 += 32) {
-    const float2 ml = k0 == 0 ? ml0 : ml_at(k0 + lane);
-    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - base_m);
-    l += ml.y * w;
-    const int n = min(32, np - k0);
-    if (k0 == 0) {
-#pragma unroll
-      for (int kk = 0; kk < kPre; ++kk) add(pre[kk], __shfl_sync(0xffffffffu, w, kk));
-    }
-    const int first = k0 == 0 ? kPre : 0;
-#pragma unroll 4
-    for (int kk = first; kk < n; ++kk)
-      add(*reinterpret_cast<const Vec*>(a + (k0 + kk) * part_stride), __shfl_sync(0xffffffffu, w, kk));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  __nv_bfloat16* dst = out + (static_cast<int64_t>(row) * g.hq + qh) * D + lane * E;
-  if constexpr (E == 4) {
-    uint2 wv;
-    wv.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-    wv.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(dst) = wv;
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
-  }
-  if (lse && lane == 0) lse[static_cast<int64_t>(row) * g.hq + qh] = (m + __log2f(l)) * 0.6931471805599453f;
+  const int4 mi = p.merge_info[wid / g.hq];  // one load: (row, parts, first part)
+  merge_parts<D>(g, out, lse, part_acc, part_ml, mi.x, mi.y, mi.z, wid % g.hq, lane);
 }
 
 template <bool E4M3, int D, bool CAP, int NTW>

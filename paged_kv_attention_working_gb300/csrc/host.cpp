@@ -115,6 +115,13 @@ struct pie_ctx {
   bool upload_pending = false;
   float* d_part = nullptr;  // partial (acc | m,l) results
   size_t part_cap = 0;      // floats
+  // per (merged row, query head): parts stored so far, for the decode
+  // kernels' own merge; zero between launches (each row's last part resets
+  // its counters), cleared again after a failed launch
+  int32_t* d_cnt = nullptr;
+  size_t cnt_cap = 0;       // counters
+  bool cnt_dirty = false;
+  int32_t merge_mode = 0;   // pie_ctx_set_merge_mode
   pie_batch* open = nullptr;
   bool fail_next_begin = false;  // self-test: fake a CUDA failure at the plan upload
 };
@@ -190,7 +197,7 @@ pie_status ensure_device(pie_ctx* c, T** buf, size_t* cap, size_t need) {
 
 // -------------------------------------------------------------- planner
 struct PlanBuilder {
-  std::vector<int32_t> page_ids, row_pos, row_slot, row_part_base, row_list;
+  std::vector<int32_t> page_ids, row_pos, row_slot, row_part_base, row_list, row_merge;
   std::vector<int4> merge_info;
   std::vector<CopyItem> copies;
   std::vector<WorkItem> dec, pre;
@@ -430,9 +437,11 @@ void build_plan(pie_ctx* c, const std::vector<SegInfo>& segs_in, int32_t n_rows,
   // part bases: rows with a single part are written directly
   int32_t total = 0;
   pb.row_part_base.assign(n_rows, -1);
+  pb.row_merge.assign(n_rows, -1);
   for (int32_t r = 0; r < n_rows; ++r) {
     if (n_parts[r] >= 2) {
       pb.row_part_base[r] = total;
+      pb.row_merge[r] = static_cast<int32_t>(pb.merge_info.size());
       total += n_parts[r];
       pb.merge_info.push_back(make_int4(r, n_parts[r], pb.row_part_base[r], 0));
     }
@@ -604,6 +613,7 @@ pie_status pie_ctx_destroy(pie_ctx* c) {
     if (c->d_err) cudaFree(c->d_err);
     if (c->d_plan) cudaFree(c->d_plan);
     if (c->d_part) cudaFree(c->d_part);
+    if (c->d_cnt) cudaFree(c->d_cnt);
     if (c->h_plan) cudaFreeHost(c->h_plan);
     if (c->upload_done) cudaEventDestroy(c->upload_done);
     if (c->side) {
@@ -832,7 +842,7 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
   std::vector<uint8_t> blob;
   size_t o_pages = put(blob, pb.page_ids), o_pos = put(blob, pb.row_pos), o_slot = put(blob, pb.row_slot);
   size_t o_base = put(blob, pb.row_part_base), o_list = put(blob, pb.row_list);
-  size_t o_mi = put(blob, pb.merge_info);
+  size_t o_mi = put(blob, pb.merge_info), o_rm = put(blob, pb.row_merge);
   size_t o_cp = put(blob, pb.copies), o_dec = put(blob, pb.dec, 32), o_pre = put(blob, pb.pre, 32);
   int64_t total_parts = 0;
   for (const int4& mi : pb.merge_info) total_parts += mi.y;
@@ -850,6 +860,11 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     v.max_dec_m = std::max(v.max_dec_m, m);
     v.n_dec_wide += m > pie::kDecodeNarrowM;
   }
+  // Merge mode 1: the decode kernels merge split rows themselves when every
+  // part comes from a decode item (the tensor-core kernel does not count its
+  // parts); otherwise, and by default, a merge launch follows.
+  bool fused_merge = v.n_merge > 0 && !c->plan_only && c->merge_mode == 1;
+  for (const WorkItem& it : pb.pre) fused_merge = fused_merge && it.part < 0;
   if (c->fail_next_begin) {
     c->fail_next_begin = false;
     undo_reservation(c, undo);
@@ -860,6 +875,16 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     pie_status st = ensure_device(c, &c->d_plan, &c->plan_cap, blob.size());
     size_t part_need = static_cast<size_t>(total_parts) * c->geo.hq * (c->geo.d + 2);
     if (st == PIE_OK) st = ensure_device(c, &c->d_part, &c->part_cap, std::max<size_t>(part_need, 1));
+    const size_t cnt_need = static_cast<size_t>(v.n_merge) * c->geo.hq;
+    if (st == PIE_OK && fused_merge && cnt_need > c->cnt_cap) {
+      st = ensure_device(c, &c->d_cnt, &c->cnt_cap, cnt_need);
+      c->cnt_dirty = true;  // a new buffer is not zeroed yet
+    }
+    if (st == PIE_OK && fused_merge && c->cnt_dirty) {
+      cudaError_t e = cudaMemsetAsync(c->d_cnt, 0, c->cnt_cap * sizeof(int32_t), c->stream);
+      if (e != cudaSuccess) st = cuda_fail(c, e, "cudaMemsetAsync");
+      else c->cnt_dirty = false;
+    }
     if (st == PIE_OK && c->upload_pending) {
       cudaError_t e = cudaEventSynchronize(c->upload_done);
       if (e != cudaSuccess) st = cuda_fail(c, e, "cudaEventSynchronize");
@@ -893,6 +918,8 @@ pie_status pie_batch_begin(pie_ctx* c, const pie_seg* segs, int32_t n_segs, pie_
     v.row_part_base = reinterpret_cast<const int32_t*>(d + o_base);
     v.row_list = reinterpret_cast<const int32_t*>(d + o_list);
     v.merge_info = reinterpret_cast<const int4*>(d + o_mi);
+    v.row_merge = reinterpret_cast<const int32_t*>(d + o_rm);
+    v.merge_cnt = fused_merge ? c->d_cnt : nullptr;
     v.copies = reinterpret_cast<const CopyItem*>(d + o_cp);
     v.dec_items = reinterpret_cast<const WorkItem*>(d + o_dec);
     v.pre_items = reinterpret_cast<const WorkItem*>(d + o_pre);
@@ -1073,8 +1100,17 @@ pie_status pie_attend(pie_ctx* c, pie_batch* b, int32_t layer, const void* q, vo
                            out, lse, acc, ml, c->d_err, other);
   if (e == cudaSuccess && side) e = cudaEventRecord(c->join_ev, c->side);
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(c->stream, c->join_ev, 0);
-  if (e == cudaSuccess && v.n_merge) e = pie::launch_merge(c->geo, v, out, lse, acc, ml, c->stream);
-  if (e != cudaSuccess) return cuda_fail(c, e, "attend launch");
+  if (e == cudaSuccess && v.n_merge && !v.merge_cnt) e = pie::launch_merge(c->geo, v, out, lse, acc, ml, c->stream);
+  if (e != cudaSuccess) {
+    c->cnt_dirty = true;  // some parts may be counted without their row's merge
+    return cuda_fail(c, e, "attend launch");
+  }
+  return PIE_OK;
+}
+
+pie_status pie_ctx_set_merge_mode(pie_ctx* c, int32_t mode) {
+  if (!c || mode < 0 || mode > 1) return PIE_ERR_INVALID;
+  c->merge_mode = mode;
   return PIE_OK;
 }
 
@@ -1085,6 +1121,7 @@ pie_status pie_ctx_check(pie_ctx* c, int32_t* flags) {
   cudaError_t e = cudaStreamSynchronize(c->stream);
   if (e == cudaSuccess) e = cudaMemcpy(flags, c->d_err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int));
+  if (e == cudaSuccess && *flags) c->cnt_dirty = true;  // the next pass clears the merge counters
   if (e != cudaSuccess) return cuda_fail(c, e, "pie_ctx_check");
   return PIE_OK;
 }
@@ -1109,6 +1146,7 @@ pie_status pie_batch_plan_info(const pie_batch* b, int32_t* info) {
   info[1] = b->view.n_pre;
   info[2] = b->view.n_merge;
   info[3] = b->view.n_copies;
+  info[4] = b->view.n_merge > 0 && !b->view.merge_cnt;
   return PIE_OK;
 }
 

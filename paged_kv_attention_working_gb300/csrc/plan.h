@@ -43,6 +43,12 @@ struct PlanView {
   const WorkItem* pre_items;     // tensor-core (prefill) items
   const int4* merge_info;        // rows with >= 2 parts: (row, parts, first
                                  // part index = row_part_base[row], 0)
+  const int32_t* row_merge;      // [n_rows]: index into merge_info, -1 for direct rows
+  int32_t* merge_cnt;            // [n_merge][Hq] parts stored so far, zero
+                                 // between launches; non-null: the decode
+                                 // kernels merge split rows themselves (no
+                                 // tensor-core item writes partials), else a
+                                 // merge launch follows
   const CopyItem* copies;
   int32_t n_rows, n_dec, n_pre, n_merge, n_copies;
   int32_t max_dec_m;             // largest rows x query heads of a decode item

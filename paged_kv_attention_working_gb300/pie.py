@@ -30,7 +30,7 @@ EXPORTS = [
     "pie_ws_page_table", "pie_page_refcount", "pie_free_pages", "pie_batch_begin", "pie_batch_rows",
     "pie_batch_slots", "pie_kv_append", "pie_attend", "pie_batch_end", "pie_batch_plan_info",
     "pie_batch_items", "pie_ctx_check", "pie_attend_decode_noalloc", "pie_selftest_wait_timeout",
-    "pie_kv_append_rope", "pie_rope_table", "pie_selftest_fail_next_begin",
+    "pie_kv_append_rope", "pie_rope_table", "pie_selftest_fail_next_begin", "pie_ctx_set_merge_mode",
 ]
 PIE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -101,6 +101,7 @@ def _load():
         "pie_attend_decode_noalloc": [P(pie_decode_args)],
         "pie_selftest_wait_timeout": [V, I],
         "pie_selftest_fail_next_begin": [V],
+        "pie_ctx_set_merge_mode": [V, I],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -178,6 +179,12 @@ def pie_ctx_check(ctx) -> int:
     v = ctypes.c_int32()
     _check(ctx, lib.pie_ctx_check(ctx, ctypes.byref(v)), "pie_ctx_check")
     return v.value
+
+
+def pie_ctx_set_merge_mode(ctx, mode) -> None:
+    """0: split rows merged by a merge launch (the default); 1: inside the
+    decode launches when no tensor-core item is split."""
+    _check(ctx, lib.pie_ctx_set_merge_mode(ctx, mode), "pie_ctx_set_merge_mode")
 
 
 def pie_selftest_wait_timeout(ctx, polls) -> None:
@@ -277,9 +284,10 @@ def pie_batch_slots(batch):
 
 
 def pie_batch_plan_info(batch):
-    info = (ctypes.c_int32 * 4)()
+    info = (ctypes.c_int32 * 5)()
     _check(None, lib.pie_batch_plan_info(batch, info), "pie_batch_plan_info")
-    return {"decode_items": info[0], "prefill_items": info[1], "merge_rows": info[2], "copies": info[3]}
+    return {"decode_items": info[0], "prefill_items": info[1], "merge_rows": info[2], "copies": info[3],
+            "merge_launch": info[4]}
 
 
 def pie_batch_items(batch, kind):

@@ -39,10 +39,15 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-def _parity(name, num_sms=0):
+def _parity(name, num_sms=0, before=None):
+    """Runs reduced workload `name` on the device and the oracle and compares
+    pools, outputs and LSE; before(ctx) runs first.  Returns the device
+    passes' plan summaries."""
     w = wl.reduced(name)
     store, handles, ref_passes = oracle_driver.run(w)
     g = gpu_driver.DeviceRun(w, num_sms=num_sms)
+    if before is not None:
+        before(g.ctx)
     passes = g.run()
     kp, vp = g.pools()
     np.testing.assert_array_equal(kp, store.pool[0])
@@ -57,6 +62,7 @@ def _parity(name, num_sms=0):
             lse = got["lse"][layer].cpu().numpy()
             assert_close(lse, ref["lse"][layer], LSE_ATOL, 0.0, f"{name} lse layer {layer}")
     g.close()
+    return [p["plan"] for p in passes]
 
 
 @pytest.mark.parametrize("name", list(wl.FULL) + list(wl.EXTRA))
@@ -73,6 +79,46 @@ def test_reduced_workload_parity(name):
                                   "interleaved_forks"])
 def test_reduced_workload_parity_few_sms(name):
     _parity(name, num_sms=2)
+
+
+# Workloads whose split rows come from decode items only (one per kernel
+# variant: bf16 and e4m3 pages, d 64, wide fork / dedup items, G 64), plus
+# the fork workload, which runs passes with split tensor-core items (merge
+# launch) and then decode-only passes.
+MERGE_CASES = ["llama8b_decode", "llama70b_fp8", "mixed_batch_e4m3", "mixed_batch_d64", "edge_batch",
+               "mixed_batch_mqa_g64", "fork_spec"]
+
+
+@pytest.mark.parametrize("name", MERGE_CASES)
+def test_split_rows_merged_inside_the_decode_launch(name):
+    """Mode 1: rows split over decode items only are combined by the decode
+    kernels themselves (per (row, query head) a count of stored parts; the
+    CTA that stores the last part merges them and resets the count), with no
+    merge launch; passes with a split tensor-core item still take one.
+    Consecutive attends (two layers, or several passes) must each leave the
+    counts at zero, and a kernel error report first makes the next pass clear
+    them.  Against the oracle."""
+    def setup(ctx):
+        pie.pie_ctx_set_merge_mode(ctx, 1)
+        pie.pie_selftest_wait_timeout(ctx, 64)
+        assert pie.pie_ctx_check(ctx) == 1
+
+    merged = [p for p in _parity(name, before=setup) if p["merge_rows"]]
+    assert any(not p["merge_launch"] for p in merged)
+    if name == "fork_spec":  # its first passes split the shared prompt's tensor-core items
+        assert any(p["merge_launch"] for p in merged)
+
+
+@pytest.mark.parametrize("name", ["llama70b_fp8", "fork_spec"])
+def test_split_rows_merged_by_a_merge_launch_by_default(name):
+    """Mode 0, the default: every pass with split rows ends with a merge
+    launch (set explicitly here after mode 1, to check the switch back)."""
+    def setup(ctx):
+        pie.pie_ctx_set_merge_mode(ctx, 1)
+        pie.pie_ctx_set_merge_mode(ctx, 0)
+
+    merged = [p for p in _parity(name, before=setup) if p["merge_rows"]]
+    assert merged and all(p["merge_launch"] for p in merged)
 
 
 @pytest.mark.parametrize("scale", [5.0 / 448.0, 0.37, 1.0])

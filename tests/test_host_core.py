@@ -386,6 +386,17 @@ def test_plan_only_context_rejects_device_calls():
     pie.pie_ctx_destroy(c)
 
 
+def test_merge_mode_takes_the_two_documented_values():
+    c = pie.pie_ctx_create(1, 4, 2, 64, 8)
+    for mode in (0, 1):
+        pie.pie_ctx_set_merge_mode(c, mode)
+    for mode in (-1, 2):
+        with pytest.raises(pie.PieError) as e:
+            pie.pie_ctx_set_merge_mode(c, mode)
+        assert e.value.status == pie.PIE_ERR_INVALID
+    pie.pie_ctx_destroy(c)
+
+
 def test_invalid_configurations_rejected():
     with pytest.raises(pie.PieError):
         pie.pie_ctx_create(1, 6, 4, 64, 8)           # Hq not a multiple of Hkv
