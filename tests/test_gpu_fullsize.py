@@ -103,19 +103,21 @@ def row_ranges(segs):
     return out
 
 
-def check(w, names, layers, rows_of=None):
+def check(w, names, layers, rows_of=None, merge_mode=0):
     """Runs w on the GPU (names exact) and the restricted script on the
-    oracle; compares pool bytes and attention rows of the named sets."""
+    oracle; compares pool bytes and attention rows of the named sets.
+    Returns the device passes' plan summaries."""
+    from paged_kv_attention_working_gb300 import pie
     sub = sub_workload(w, names)
     store, ohandles, ref_passes = oracle_driver.run(sub, layers=layers, kv_layers=layers)
     g = gpu_driver.DeviceRun(w)
+    pie.pie_ctx_set_merge_mode(g.ctx, merge_mode)
     passes = g.run(layers=layers, kv_source=exact_source(w, set(names)))
     # appended bytes, page by page in logical order, valid slots only
     esize = 2 if w.kv_dtype == wl.KV_BF16 else 1
     offs = kvstore.block_offsets(16, w.head_dim, esize)
     shape = (w.num_layers, w.num_pages, w.num_kv_heads, g.block)
     kp, vp = g.kpool.view(shape), g.vpool.view(shape)
-    from paged_kv_attention_working_gb300 import pie
     for n in names:
         n_tok = pie.pie_ws_info(g.ctx, g.handles[n])[0]
         gpages = pie.pie_ws_page_table(g.ctx, g.handles[n])
@@ -145,6 +147,7 @@ def check(w, names, layers, rows_of=None):
                 lse = got["lse"][layer][a:b].cpu().numpy()[sel]
                 assert np.abs(lse - ref["lse"][layer][c:d][sel]).max() <= LSE_ATOL, f"{n} lse layer {layer}"
     g.close()
+    return [p["plan"] for p in passes]
 
 
 def test_llama8b_decode_full():
@@ -205,3 +208,22 @@ def test_llama8b_decode_full_rope():
     order = np.argsort(w.ctx)
     names = [f"w{order[0]}", f"w{order[-1]}"]
     check(w, names, layers=[0])
+
+
+@pytest.mark.parametrize("name", ["llama8b_decode", "llama70b_fp8"])
+def test_decode_full_merged_inside_the_decode_launch(name):
+    """Merge mode 1 at the benchmark's sizes: the decode kernels merge the
+    split rows themselves (per (row, query head) part counters: 64 x 32 and
+    256 x 64 of them, over several waves of CTAs; for the 70B batch the wide
+    and narrow launches count into the same counters), with no merge launch.
+    The 8B batch attends two layers of the pass, so the counters must be back
+    at zero after the first."""
+    w = getattr(wl, name)()
+    if name == "llama8b_decode":
+        order = np.argsort(w.ctx)
+        names, layers = [f"w{order[0]}", f"w{order[len(order) // 2]}", f"w{order[-1]}"], [0, w.num_layers - 1]
+    else:
+        names, layers = [f"w{i}" for i in range(248, 256)], [0]
+    plans = check(w, names, layers=layers, merge_mode=1)
+    decode_passes = [p for p in plans if p["merge_rows"]]
+    assert decode_passes and not any(p["merge_launch"] for p in decode_passes)
