@@ -265,8 +265,7 @@ def run_reference(args, w, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(per_step), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "n_ws": len(w.ctx), "layers": w.num_layers, "hq": w.num_q_heads,
-                       "hkv": w.num_kv_heads, "head_dim": w.head_dim, "kv_dtype": "bf16"},
+            "config": decode_config(args, w, world),
             "rows_per_s": rps,
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -287,6 +286,18 @@ def decode_attend_bytes(w):
     pages = sum(-(-(c + 1) // 16) for c in w.ctx) - shared // 16
     kv = keys * Hkv * D * esize * 2
     return kv, kv + 2 * n_rows * Hq * D * 2 + n_rows * Hq * 4 + 4 * pages
+
+
+def decode_config(args, w, world):
+    """The config of a decode workload's line, the same for the GPU arm and
+    the oracle arm."""
+    kv, _ = decode_attend_bytes(w)
+    return {"workload": w.name, "n_ws": len(w.ctx), "contexts": "uniform [%d, %d] seeded" % w.ctx_range,
+            "layers": w.num_layers, "hq": w.num_q_heads, "hkv": w.num_kv_heads, "head_dim": w.head_dim,
+            "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3", "page_size": 16,
+            "l2": "inputs larger than L2 (%.1f GB of K/V per layer)" % (kv / 1e9),
+            "logit_softcap": args.logit_softcap, "rope_theta": args.rope_theta, "merge_mode": args.merge_mode,
+            "parallelism": f"replicas x{world}"}
 
 
 def prefill_chunk_flops(w, chunk_segs):
@@ -476,12 +487,7 @@ def run_gpu(args, w, world, rank, local, e2e=True):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == 0 else "e4m3 KV, bf16 Q/O",
         "data": "synthetic",
-        "config": {"workload": w.name, "n_ws": n_rows, "contexts": "uniform [%d, %d] seeded" % w.ctx_range,
-                   "layers": L,
-                   "hq": Hq, "hkv": Hkv, "head_dim": D, "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3",
-                   "page_size": 16, "l2": "inputs larger than L2 (~1.1 GB KV per layer)",
-                   "logit_softcap": args.logit_softcap, "rope_theta": args.rope_theta,
-                   "merge_mode": args.merge_mode, "parallelism": f"replicas x{world}"},
+        "config": decode_config(args, w, world),
         "rows_per_s": world * n_rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+merge) per pie_attend",
                      "achieved": achieved, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
